@@ -1,0 +1,264 @@
+"""Python binding of libfp8blk.so, the block-scaled FP8 linear layer for GB300.
+
+Argument marshalling only: every function hands device pointers, sizes and
+strides of PyTorch tensors to the C ABI declared in include/fp8blk.h, on the
+current CUDA stream unless one is given.  Every step of the computation runs
+in the library's CUDA kernels; there is no Python or CPU fallback, and the
+first call raises ImportError when the library has not been built.
+
+Functions named ``fp8blk_*`` mirror the C entry points one to one and write
+into caller-provided tensors.  The short names (``quant_act``, ``gemm_w8a8``,
+...) allocate their outputs and call the same entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8blk.so")
+
+SCALE_F32_128x128 = 0
+SCALE_UE8M0_32x32 = 1
+
+STATUS_NAMES = {
+    0: "FP8BLK_OK",
+    1: "FP8BLK_ERR_INVALID_ARG",
+    2: "FP8BLK_ERR_UNSUPPORTED_SHAPE",
+    3: "FP8BLK_ERR_MISALIGNED",
+    4: "FP8BLK_ERR_ARCH",
+    5: "FP8BLK_ERR_CUDA",
+    6: "FP8BLK_ERR_NAN_CODE",
+    7: "FP8BLK_ERR_SCALE_WINDOW",
+    8: "FP8BLK_ERR_TIMEOUT",
+}
+
+# Every symbol the header declares: name -> (restype, argtypes).
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+EXPORTS = {
+    "fp8blk_quant_act": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
+    "fp8blk_gemm_w8a8": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "fp8blk_gemm_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _P]),
+    "fp8blk_gemv_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _P]),
+    "fp8blk_quant_weight": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "fp8blk_validate_weights": (_I32, [_P, _I64, _P, _I32, _I64, _I64, _P, _P]),
+    "fp8blk_debug_decode_e4m3": (_I32, [_P, _I64, _I32, _P, _P]),
+    "fp8blk_query_constraints": (_I32, [_P]),
+    "fp8blk_status_string": (ctypes.c_char_p, [_I32]),
+    "fp8blk_device_error": (_I32, [_P, _I32]),
+}
+
+
+class Constraints(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "abi_version", "scale_block_k", "scale_block_n", "ue8m0_block", "w8a8_tile_m", "w8a8_tile_n",
+        "w8a16_tile_n", "w8a16_max_tile_m", "gemv_max_m", "ptr_align_bytes", "row_align_bytes",
+        "lds_multiple", "max_split_k")]
+
+
+class Fp8BlkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        msg = _L().fp8blk_status_string(self.status).decode()
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.status, self.status)} ({msg})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -m block_scaled_fp8_bf16_gb300.build` "
+            "(or __graft_entry__.build()) first")
+    handle = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in EXPORTS.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
+lib = None
+
+
+def _L():
+    """The loaded library (loaded on first use; raises ImportError when it is
+    not built, so no call can silently run anything else)."""
+    global lib
+    if lib is None:
+        lib = _load()
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise Fp8BlkError(status, where)
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ld(t):
+    """Row pitch in elements of a 2-D tensor whose last dimension is contiguous."""
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("last dimension must be contiguous")
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
+
+
+def _bytes_tensor(t):
+    import torch
+    return t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t
+
+
+def _expect(t, dtypes, name):
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+
+
+# ---------------------------------------------------------------- C entry points
+
+def fp8blk_quant_act(x, a, a_scales, stream=None):
+    """x [M, K] bf16 -> a [M, K] e4m3 (uint8 view), a_scales [K/128, lds] fp32."""
+    import torch
+    _expect(x, (torch.bfloat16,), "x")
+    a = _bytes_tensor(a)
+    M, K = x.shape
+    _check(_L().fp8blk_quant_act(_ptr(x), M, K, _ld(x), _ptr(a), _ld(a), _ptr(a_scales), _ld(a_scales),
+                                _stream(stream)), "fp8blk_quant_act")
+
+
+def fp8blk_gemm_w8a8(a, a_scales, b, b_scales, c, stream=None):
+    """C[M, N] bf16 = block-scaled a[M, K] e4m3 x b[N, K] e4m3."""
+    a, b = _bytes_tensor(a), _bytes_tensor(b)
+    M, K = a.shape
+    N = b.shape[0]
+    _check(_L().fp8blk_gemm_w8a8(_ptr(a), _ld(a), _ptr(a_scales), _ld(a_scales), _ptr(b), _ld(b), _ptr(b_scales),
+                                _ptr(c), _ld(c), M, N, K, _stream(stream)), "fp8blk_gemm_w8a8")
+
+
+def fp8blk_gemm_w8a16(x, b, b_scales, fmt, c, stream=None):
+    """C[M, N] bf16 = x[M, K] bf16 x b[N, K] e4m3 with fp32 128x128 or UE8M0 32x32 scales."""
+    b = _bytes_tensor(b)
+    M, K = x.shape
+    N = b.shape[0]
+    _check(_L().fp8blk_gemm_w8a16(_ptr(x), _ld(x), _ptr(b), _ld(b), _ptr(b_scales), int(fmt), _ptr(c), _ld(c),
+                                 M, N, K, _stream(stream)), "fp8blk_gemm_w8a16")
+
+
+def fp8blk_gemv_w8a16(x, b, b_scales, fmt, c, stream=None):
+    """Decode-size (M <= 16) form of fp8blk_gemm_w8a16."""
+    b = _bytes_tensor(b)
+    M, K = x.shape
+    N = b.shape[0]
+    _check(_L().fp8blk_gemv_w8a16(_ptr(x), _ld(x), _ptr(b), _ld(b), _ptr(b_scales), int(fmt), _ptr(c), _ld(c),
+                                 M, N, K, _stream(stream)), "fp8blk_gemv_w8a16")
+
+
+def fp8blk_quant_weight(w, b, b_scales, stream=None):
+    """w [N, K] bf16 -> b [N, K] e4m3, b_scales [N/128, K/128] fp32 (packed)."""
+    b = _bytes_tensor(b)
+    N, K = w.shape
+    _check(_L().fp8blk_quant_weight(_ptr(w), N, K, _ld(w), _ptr(b), _ld(b), _ptr(b_scales), _stream(stream)),
+           "fp8blk_quant_weight")
+
+
+def fp8blk_validate_weights(b, b_scales, fmt, dev_counts, stream=None):
+    b = _bytes_tensor(b)
+    N, K = b.shape
+    _check(_L().fp8blk_validate_weights(_ptr(b), _ld(b), _ptr(b_scales), int(fmt), N, K, _ptr(dev_counts),
+                                       _stream(stream)), "fp8blk_validate_weights")
+
+
+def fp8blk_debug_decode_e4m3(codes, exp_shift, out, stream=None):
+    _check(_L().fp8blk_debug_decode_e4m3(_ptr(codes), codes.numel(), int(exp_shift), _ptr(out), _stream(stream)),
+           "fp8blk_debug_decode_e4m3")
+
+
+def fp8blk_query_constraints() -> dict:
+    c = Constraints()
+    _check(_L().fp8blk_query_constraints(ctypes.byref(c)), "fp8blk_query_constraints")
+    return {n: getattr(c, n) for n, _ in Constraints._fields_}
+
+
+def fp8blk_device_error(clear: bool = False) -> int:
+    """Raw device error word (0 = none).  Synchronises the device."""
+    code = ctypes.c_int32(0)
+    st = _L().fp8blk_device_error(ctypes.byref(code), 1 if clear else 0)
+    if st not in (0, 8):
+        _check(st, "fp8blk_device_error")
+    return int(code.value)
+
+
+# ---------------------------------------------------------------- allocating helpers
+
+def act_scales_pitch(M: int) -> int:
+    return (M + 3) // 4 * 4
+
+
+def quant_act(x, stream=None):
+    import torch
+    M, K = x.shape
+    a = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((K // 128, act_scales_pitch(M)), dtype=torch.float32, device=x.device)
+    fp8blk_quant_act(x, a, s, stream)
+    return a, s
+
+
+def quant_weight(w, stream=None):
+    import torch
+    N, K = w.shape
+    b = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
+    fp8blk_quant_weight(w, b, s, stream)
+    return b, s
+
+
+def gemm_w8a8(a, a_scales, b, b_scales, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[0]), dtype=torch.bfloat16, device=a.device)
+    fp8blk_gemm_w8a8(a, a_scales, b, b_scales, out, stream)
+    return out
+
+
+def gemm_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty((x.shape[0], b.shape[0]), dtype=torch.bfloat16, device=x.device)
+    fp8blk_gemm_w8a16(x, b, b_scales, fmt, out, stream)
+    return out
+
+
+def gemv_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty((x.shape[0], b.shape[0]), dtype=torch.bfloat16, device=x.device)
+    fp8blk_gemv_w8a16(x, b, b_scales, fmt, out, stream)
+    return out
+
+
+def linear_w8a8(x, b, b_scales, out=None, stream=None):
+    """bf16 x -> per-token quantisation -> W8A8 GEMM (two launches)."""
+    a, s = quant_act(x, stream)
+    return gemm_w8a8(a, s, b, b_scales, out, stream)
+
+
+def validate_weights(b, b_scales, fmt=SCALE_F32_128x128, stream=None):
+    """(nan_code_count, bad_scale_count); synchronises the stream."""
+    import torch
+    counts = torch.empty(2, dtype=torch.int32, device=b.device)
+    fp8blk_validate_weights(b, b_scales, fmt, counts, stream)
+    c = counts.cpu()
+    return int(c[0]), int(c[1])

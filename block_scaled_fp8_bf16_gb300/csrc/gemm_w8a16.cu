@@ -1,0 +1,464 @@
+// W8A16 GEMM for sm_103a: bf16 activations x e4m3 weights, FP32 accumulate.
+//
+// There is no bf16 x e4m3 tensor-core instruction, so the weights are decoded
+// to bf16 and the product runs as bf16 x bf16 MMA ("FP8 / NVFP4 weight-only
+// inference on the RTX 3090 loses nothing", section 2; the Blackwell kernel
+// it quotes decodes to BF16 and issues BF16 tcgen05 MMA).
+//
+// The problem is computed transposed, C^T[n, m] = sum_k W[n, k] X[m, k]: a
+// 128-row weight tile is the MMA's M side and a token tile of TM = 16..128
+// rows is the MMA's N side, so decode-size batches still fill the 128-row
+// tensor-core operand.  The decoded weights go straight from registers into
+// tensor memory (tcgen05.st) and feed the MMA as its TMEM-resident A operand,
+// so shared memory only carries the raw e4m3 tile and the activation tile:
+//
+//   warp 0      TMA producer: e4m3 weight tile [128 n x 128 k] (16 KB) and
+//               bf16 activation tile [TM x 128 k] per 128-K block.
+//   warp 1      TMEM allocation; one thread issues eight tcgen05.mma
+//               kind::f16 (K = 16) per K block, A from TMEM, B from smem.
+//   warps 2..5  decode: thread = weight row; reads its 128 codes, decodes them
+//               exactly to bf16 (integer ops + one packed multiply, see
+//               decode.cuh) and stores them to one of two TMEM A buffers.
+//   warps 6..9  epilogue: thread = weight row n, TM accumulators (tokens).
+//
+// Scale formats:
+//   fp32 128x128: one FP32 partial per 128-K block in TMEM (double buffered),
+//     promoted once per block as acc += partial * Bs[n/128, kb]
+//     ("perf(ArcKernels) ...", "What this adds": promote at every scale-block
+//     boundary along K).
+//   UE8M0 32x32: the power of two 2^e of each 32x32 block is folded exactly
+//     into the decode multiplier, so the whole K range accumulates in TMEM
+//     and the epilogue only converts ("SM70 FP8 block-32 kernels (PLI Labs)",
+//     "Exactness").
+//
+// Tiles run persistently; when the tile count cannot fill the GPU, K is split
+// over a 2..8-CTA cluster and the FP32 partial tiles are summed in rank order
+// through distributed shared memory by rank 0.
+#include <cuda_bf16.h>
+
+#include "decode.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8blk {
+namespace {
+
+constexpr int BN = kW8A16TileN;   // weight rows per tile (MMA M)
+constexpr int BK = 128;           // K per block (one fp32 scale block)
+constexpr int kStageW = BN * BK;  // 16 KB of e4m3
+constexpr int kDecWarps = 4;
+constexpr int kACols = BK / 2;    // TMEM columns of one decoded A block (2 bf16 per column)
+constexpr int kGroupN = 8;
+constexpr int kBarrierBytes = 512;
+
+template <int TM>
+struct Cfg {
+  // Epilogue warps: 4 (one per TMEM lane quarter) or 8 for the widest token
+  // tile, where two warps share a lane quarter and split the columns.
+  static constexpr int kEpiWarps = TM >= 128 ? 8 : 4;
+  static constexpr int kEpiCols = TM / (kEpiWarps / 4);
+  static constexpr int kThreads = 64 + (kDecWarps + kEpiWarps) * 32;
+  static constexpr int kStageX = TM * BK * 2;                  // bf16 activation tile
+  static constexpr int kStageBytes = kStageW + kStageX;
+  // One CTA per SM (registers are allocated per 4-warp group, so a second
+  // 10..14-warp CTA would not fit); the ring is as deep as shared memory allows.
+  static constexpr int kStages = TM == 16 ? 8 : (TM == 32 ? 7 : (TM == 64 ? 5 : 4));
+  static constexpr uint32_t kTmemUsed = 2 * kACols + 2 * TM;
+  static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+  static constexpr uint32_t kIdesc = make_idesc(1 /* bf16 */, BN, TM);
+  static constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + kBarrierBytes + 1024;
+  static constexpr int kMinBlocks = 1;
+  static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "tcgen05 N for M = 128");
+  static_assert(kStageX % 1024 == 0, "activation tile must keep 1024-B swizzle alignment");
+  static_assert(kTmemUsed <= 512, "TMEM budget");
+  static_assert(size_t(kStages) * kStageBytes >= size_t(TM) * BN * 4, "reduction buffer fits in the stages");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kMinBlocks == 1 || 2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM must fit");
+};
+
+__device__ __forceinline__ void tile_coords(int t, int n_tiles, int m_tiles, int& nt, int& mt) {
+  const int per_group = kGroupN * m_tiles;
+  const int g = t / per_group;
+  const int first = g * kGroupN;
+  const int gsz = min(n_tiles - first, kGroupN);
+  const int r = t - g * per_group;
+  nt = first + r % gsz;
+  mt = r / gsz;
+}
+
+__device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, int site) {
+  *abort_flag = 1;
+  atomicCAS(err, 0, kDevErrW8A16 | site);
+}
+
+template <int COLS>
+__device__ __forceinline__ void store_col(__nv_bfloat16* __restrict__ C, int64_t ldc, int M, int m0, int n,
+                                          const float* acc) {
+#pragma unroll
+  for (int j = 0; j < COLS; ++j) {
+    if (m0 + j < M) C[size_t(m0 + j) * ldc + n] = __float2bfloat16_rn(acc[j]);
+  }
+}
+
+template <int TM>
+__global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
+    w8a16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                 const void* __restrict__ scales, int fmt, __nv_bfloat16* __restrict__ C, int64_t ldc, int M,
+                 int N, int K, int split, int* __restrict__ err) {
+  using Q = Cfg<TM>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(Q::kStages) * Q::kStageBytes);
+  uint64_t* empty = full + Q::kStages;
+  uint64_t* afull = empty + Q::kStages;
+  uint64_t* aempty = afull + 2;
+  uint64_t* dfull = aempty + 2;
+  uint64_t* dempty = dfull + 2;
+  uint64_t* drain = dempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_tiles = N / BN;
+  const int m_tiles = (M + TM - 1) / TM;
+  const int num_tiles = n_tiles * m_tiles;
+  const int kblocks = K / BK;
+  const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cluster_id = blockIdx.x / split;
+  const int num_clusters = gridDim.x / split;
+  const int kb_begin = (kblocks * rank) / split;
+  const int kb_end = (kblocks * (rank + 1)) / split;
+  const bool ue8m0 = fmt != 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Q::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecWarps + 1);   // decoders done with W, MMA done with X
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&afull[i], kDecWarps);
+      mbar_init(&aempty[i], 1);
+      mbar_init(&dfull[i], 1);
+      mbar_init(&dempty[i], Q::kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Q::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tmem_a = tmem;                 // 2 x 64 columns of decoded weights
+  const uint32_t tmem_d = tmem + 2 * kACols;    // 2 x TM columns of FP32 accumulators
+
+  constexpr int EC = Q::kEpiCols;
+  float acc[EC];
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;          // weight row within the tile (TMEM lane)
+  const int col0 = warp >= 2 + kDecWarps + 4 ? EC : 0;   // second epilogue warp of a lane quarter
+  int last_nt = 0, last_mt = 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      const uint64_t pol_w = m_tiles > 1 ? policy_evict_last() : policy_evict_first();
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        int nt, mt;
+        tile_coords(t, n_tiles, m_tiles, nt, mt);
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+          const int s = it % Q::kStages;
+          const uint32_t ph = (it / Q::kStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteProducerEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* sw = smem + size_t(s) * Q::kStageBytes;
+          uint8_t* sx = sw + kStageW;
+          mbar_arrive_expect_tx(&full[s], Q::kStageBytes);
+          tma_load_2d_hint(sw, &tmW, &full[s], kb * BK, nt * BN, pol_w);
+          tma_load_2d(sx, &tmX, &full[s], kb * BK, mt * TM);
+          tma_load_2d(sx + TM * 128, &tmX, &full[s], kb * BK + 64, mt * TM);
+        }
+      }
+      if (!ok) {
+        const uint32_t first = it > uint32_t(Q::kStages) ? it - Q::kStages : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % Q::kStages], (j / Q::kStages) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        for (int kb = kb_begin; kb < kb_end && ok; ++kb, ++it) {
+          const int s = it % Q::kStages;
+          const uint32_t ph = (it / Q::kStages) & 1u;
+          const int a = it & 1;
+          const uint32_t aph = (it >> 1) & 1u;
+          const bool first_kb = kb == kb_begin;
+          const bool last_kb = kb + 1 == kb_end;
+          // fp32 format: one accumulator buffer per K block; UE8M0: per tile.
+          const bool new_acc = !ue8m0 || first_kb;
+          const bool done_acc = !ue8m0 || last_kb;
+          const int d = acc_it & 1;
+          const uint32_t dph = (acc_it >> 1) & 1u;
+          if (new_acc && !mbar_wait(&dempty[d], dph ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaAccEmpty);
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&full[s], ph, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaFull);
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&afull[a], aph, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaAFull);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t x0 = smem_u32(smem + size_t(s) * Q::kStageBytes + kStageW);
+          const uint32_t d_tmem = tmem_d + uint32_t(d * TM);
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j) {
+            const uint32_t xa = x0 + uint32_t((j >> 2) * TM * 128 + (j & 3) * 32);
+            mma_bf16_ts(d_tmem, tmem_a + uint32_t(a * kACols + j * 8), desc_sw128_kmajor(xa), Q::kIdesc,
+                        (j > 0 || !new_acc) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+          mma_commit(&aempty[a]);
+          if (done_acc) {
+            mma_commit(&dfull[d]);
+            ++acc_it;
+          }
+        }
+      }
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else if (warp < 2 + kDecWarps) {
+    // ------------------------------------------------------------ decode
+    uint32_t it = 0;
+    bool ok = true;
+    const float* bs32 = static_cast<const float*>(scales);
+    const uint8_t* ue = static_cast<const uint8_t*>(scales);
+    (void)bs32;
+    for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      int nt, mt;
+      tile_coords(t, n_tiles, m_tiles, nt, mt);
+      const int n = nt * BN + row;
+      const uint8_t* ue_row = ue + size_t(n / 32) * (K / 32);
+      for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+        const int s = it % Q::kStages;
+        const uint32_t ph = (it / Q::kStages) & 1u;
+        const int a = it & 1;
+        const uint32_t aph = (it >> 1) & 1u;
+        // multipliers for the four 32-wide K groups of this block
+        uint32_t mul[4];
+        if (ue8m0) {
+          const uint32_t e4 = *reinterpret_cast<const uint32_t*>(ue_row + kb * 4);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int e = int((e4 >> (8 * g)) & 0xFFu) - 127;
+            mul[g] = decode_multiplier_bf16x2(e);
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) mul[g] = decode_multiplier_bf16x2(0);
+        }
+        const bool got_w = __all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag));
+        if (!got_w) {
+          raise_error(err, abort_flag, kSiteDecodeFull);
+          ok = false;
+          break;
+        }
+        // 128 codes of this row, 16 per 16-byte chunk; chunk c sits at
+        // position c ^ (row & 7) of the 128-byte swizzled row.
+        const uint8_t* wrow = smem + size_t(s) * Q::kStageBytes + row * 128;
+        uint4 raw[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(wrow + ((c ^ (row & 7)) << 4));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        const bool got_a = __all_sync(0xffffffffu, mbar_wait(&aempty[a], aph ^ 1u, abort_flag));
+        if (!got_a) {
+          raise_error(err, abort_flag, kSiteDecodeAEmpty);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_a + (uint32_t(quarter * 32) << 16) + uint32_t(a * kACols);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {            // 32 codes -> 16 TMEM columns
+          uint32_t words[16];
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const uint4 v = raw[2 * h + c2];
+            decode4_e4m3_bf16(v.x, mul[h], words[8 * c2 + 0], words[8 * c2 + 1]);
+            decode4_e4m3_bf16(v.y, mul[h], words[8 * c2 + 2], words[8 * c2 + 3]);
+            decode4_e4m3_bf16(v.z, mul[h], words[8 * c2 + 4], words[8 * c2 + 5]);
+            decode4_e4m3_bf16(v.w, mul[h], words[8 * c2 + 6], words[8 * c2 + 7]);
+          }
+          tmem_st_x16(taddr + uint32_t(h * 16), words);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[a]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ promotion + epilogue
+    uint32_t acc_it = 0;
+    bool ok = true;
+    const float* bs32 = static_cast<const float*>(scales);
+    for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      int nt, mt;
+      tile_coords(t, n_tiles, m_tiles, nt, mt);
+      last_nt = nt;
+      last_mt = mt;
+#pragma unroll
+      for (int j = 0; j < EC; ++j) acc[j] = 0.f;
+      const int kb_stop = ue8m0 ? kb_begin + 1 : kb_end;   // UE8M0: one drain per tile
+      for (int kb = kb_begin; kb < kb_stop; ++kb, ++acc_it) {
+        const int d = acc_it & 1;
+        const uint32_t dph = (acc_it >> 1) & 1u;
+        const float sc = ue8m0 ? 1.f : __ldg(bs32 + size_t(nt) * kblocks + kb);
+        const bool got = __all_sync(0xffffffffu, mbar_wait(&dfull[d], dph, abort_flag));
+        if (!got) {
+          raise_error(err, abort_flag, kSiteEpilogueFull);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_d + (uint32_t(quarter * 32) << 16) + uint32_t(d * TM + col0);
+#pragma unroll
+        for (int c = 0; c < EC / 16; ++c) {
+          uint32_t p[16];
+          tmem_ld_x16(taddr + uint32_t(c * 16), p);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(__uint_as_float(p[j]), sc, acc[c * 16 + j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[d]);
+      }
+      if (ok && split == 1) store_col<EC>(C, ldc, M, mt * TM + col0, nt * BN + row, acc);
+    }
+  }
+
+  __syncwarp();   // single-lane roles rejoin their warp before the aligned barriers below
+  if (split > 1) {
+    const bool epi = warp >= 2 + kDecWarps;
+    float* red = reinterpret_cast<float*>(smem);   // [TM][BN] floats, reuses the stages
+    if (epi && rank != 0) {
+#pragma unroll
+      for (int j = 0; j < EC; ++j) red[(col0 + j) * BN + row] = acc[j];
+    }
+    cluster_sync();
+    if (epi && rank == 0) {
+      for (int r = 1; r < split; ++r) {
+        const uint32_t base = map_shared_rank(smem_u32(red), uint32_t(r));
+#pragma unroll
+        for (int j = 0; j < EC; ++j) {
+          float v;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                       : "=f"(v)
+                       : "r"(base + uint32_t(((col0 + j) * BN + row) * 4))
+                       : "memory");
+          acc[j] += v;
+        }
+      }
+      if (!*abort_flag) store_col<EC>(C, ldc, M, last_mt * TM + col0, last_nt * BN + row, acc);
+    }
+    cluster_sync();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Q::kTmemCols);
+  }
+}
+
+template <int TM>
+cudaError_t launch_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  using Q = Cfg<TM>;
+  static bool attr_done[64] = {};
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if (device < 64 && !attr_done[device]) {
+    e = cudaFuncSetAttribute(w8a16_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Q::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done[device] = true;
+  }
+  const int n_tiles = p.N / BN;
+  const int m_tiles = (p.M + TM - 1) / TM;
+  const int tiles = n_tiles * m_tiles;
+  const int kblocks = p.K / BK;
+  const int slots = dev.num_sms * Q::kMinBlocks;
+  int split = 1;
+  if (tiles * 2 <= slots) {
+    for (int s = kMaxSplitK; s >= 2; s >>= 1) {
+      if (tiles * s <= slots && kblocks >= 2 * s) {
+        split = s;
+        break;
+      }
+    }
+  }
+  const int clusters = split > 1 ? tiles : (tiles < slots ? tiles : slots);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(clusters * split), 1, 1);
+  cfg.blockDim = dim3(Q::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Q::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w8a16_kernel<TM>, p.tmW, p.tmX, p.scales, p.fmt,
+                            static_cast<__nv_bfloat16*>(p.C), p.ldc, p.M, p.N, p.K, split, p.err);
+}
+
+}  // namespace
+
+int w8a16_pick_tile_m(int64_t M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  return 128;
+}
+
+cudaError_t launch_gemm_w8a16(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  switch (p.tile_m) {
+    case 16: return launch_tm<16>(p, dev, stream);
+    case 32: return launch_tm<32>(p, dev, stream);
+    case 64: return launch_tm<64>(p, dev, stream);
+    case 128: return launch_tm<128>(p, dev, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fp8blk

@@ -1,0 +1,356 @@
+// W8A8 block-scaled FP8 GEMM for sm_103a.
+//
+//   C[m, n] = bf16( sum_kb P[m, n, kb] * As[kb, m] * Bs[n/128, kb] ),
+//   P[m, n, kb] = sum_{k in kb} A[m, k] * B[n, k]       (e4m3 x e4m3, fp32)
+//
+// Structure ("Blockwise FP8 on Ada GPUs, part 2", "The fix"): the tensor
+// cores form one FP32 partial per 128-wide K block with no scaling inside the
+// block, and the partial is promoted once into the FP32 accumulator with
+// As * Bs.  On sm_103a the partial lives in tensor memory (TMEM), so the
+// per-slice fragments that spilled registers on Ada never exist here:
+//
+//   warp 0      TMA producer: A tile [128 x 128 B] and B tile [128 x 128 B]
+//               per 128-K block into a 6-stage shared-memory ring.
+//   warp 1      allocates 256 TMEM columns; one thread issues four
+//               tcgen05.mma kind::f8f6f4 (K = 32 each) per K block into one
+//               of two 128-column partial buffers (double buffered, so the
+//               next block's MMA overlaps this block's promotion).
+//   warps 2..9  promotion + epilogue: each thread owns one row and 64
+//               columns of the 128x128 tile; per K block it reads its partial
+//               with tcgen05.ld, releases the buffer, and does
+//               acc = fma(partial, As[kb, m] * Bs[n/128, kb], acc).
+//               At the end of the tile it rounds to bf16 and stores C.
+//
+// The weight scale is looked up per 128-wide N slice of the tile, never once
+// per CTA ("Blockwise FP8 on Ada GPUs, part 2", "The fix": the latent bug was
+// a single weight scale per thread block).  With 128-wide N tiles each tile
+// is exactly one slice.
+//
+// Large problems run persistently, one CTA per SM, over tiles in a grouped
+// raster order so that concurrently running tiles share A and B panels in L2
+// ("Blockwise FP8 on Ada GPUs, part 2", "One tile doesn't fit all M": the
+// launch-order swizzle).  Problems with too few tiles to fill the GPU split K
+// over a thread-block cluster of 2..8 CTAs; the partial accumulators are
+// summed through distributed shared memory in rank order (no global
+// workspace), and rank 0 writes C.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8blk {
+namespace {
+
+constexpr int BM = kW8A8TileM;   // 128 rows of A / C per tile
+constexpr int BN = kW8A8TileN;   // 128 rows of B (columns of C) per tile
+constexpr int BK = 128;          // one scale block of K, 128 bytes of e4m3
+constexpr int kStages = 6;
+constexpr int kStageA = BM * BK;
+constexpr int kStageB = BN * BK;
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kColsPerThread = BN / 2;   // two epilogue warps share a TMEM lane quarter
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr uint32_t kIdesc = make_idesc(0 /* e4m3 */, BM, BN);
+constexpr int kGroupM = 8;
+constexpr int kBarrierBytes = 256;
+constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + kBarrierBytes + 1024;
+
+static_assert(BK == 128, "one MMA K block must be exactly one scale block");
+static_assert(kTmemCols <= 512, "TMEM budget");
+static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 N for M = 128");
+static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "128B-swizzle atoms need 1024-B alignment");
+static_assert(2 * kStageBytes >= BM * BN * 4, "split-K reduction buffer reuses two stages");
+
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mt, int& nt) {
+  const int per_group = kGroupM * n_tiles;
+  const int g = t / per_group;
+  const int first = g * kGroupM;
+  const int gsz = min(m_tiles - first, kGroupM);
+  const int r = t - g * per_group;
+  mt = first + r % gsz;
+  nt = r / gsz;
+}
+
+__device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, int site) {
+  *abort_flag = 1;
+  atomicCAS(err, 0, kDevErrW8A8 | site);
+}
+
+__device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* acc) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < kColsPerThread / 8; ++i) {
+    uint4 v;
+    v.x = pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]);
+    v.y = pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]);
+    v.z = pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]);
+    v.w = pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]);
+    d[i] = v;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const float* __restrict__ As, int64_t lds, const float* __restrict__ Bs,
+                __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N, int K, int split,
+                int* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* dfull = empty + kStages;
+  uint64_t* dempty = dfull + 2;
+  uint64_t* drain = dempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = (M + BM - 1) / BM;
+  const int n_tiles = N / BN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int kblocks = K / BK;
+  const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cluster_id = blockIdx.x / split;
+  const int num_clusters = gridDim.x / split;
+  const int kb_begin = (kblocks * rank) / split;
+  const int kb_end = (kblocks * (rank + 1)) / split;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&dfull[d], 1);
+      mbar_init(&dempty[d], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  // Accumulator of the epilogue threads; kept live across the split-K
+  // reduction after the tile loop.
+  float acc[kColsPerThread];
+  const int quarter = warp & 3;
+  const int half = (warp - 2) >> 2;
+  const int row_in_tile = quarter * 32 + lane;
+  int last_mt = 0, last_nt = 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      // Weights are re-read by every row tile when there are several; with a
+      // single row tile they stream through once.
+      const uint64_t pol_b = m_tiles > 1 ? policy_evict_last() : policy_evict_first();
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        int mt, nt;
+        tile_coords(t, m_tiles, n_tiles, mt, nt);
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteProducerEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + size_t(s) * kStageBytes;
+          uint8_t* sb = sa + kStageA;
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tma_load_2d(sa, &tmA, &full[s], kb * BK, mt * BM);
+          tma_load_2d_hint(sb, &tmB, &full[s], kb * BK, nt * BN, pol_b);
+        }
+      }
+      if (!ok) {
+        // Let every copy this thread issued land before the CTA can exit.
+        const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++it, ++acc_it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          const int d = acc_it & 1;
+          const uint32_t dph = (acc_it >> 1) & 1u;
+          if (!mbar_wait(&dempty[d], dph ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaAccEmpty);
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&full[s], ph, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaFull);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + size_t(s) * kStageBytes);
+          const uint32_t b0 = a0 + kStageA;
+          const uint32_t d_tmem = tmem + uint32_t(d * BN);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            mma_f8_ss(d_tmem, desc_sw128_kmajor(a0 + 32u * k), desc_sw128_kmajor(b0 + 32u * k), kIdesc,
+                      k > 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+          mma_commit(&dfull[d]);
+        }
+      }
+      // No MMA may still be running when TMEM is released.
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ promotion + epilogue
+    uint32_t acc_it = 0;
+    bool ok = true;
+    for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      int mt, nt;
+      tile_coords(t, m_tiles, n_tiles, mt, nt);
+      last_mt = mt;
+      last_nt = nt;
+      const int m = mt * BM + row_in_tile;
+      const bool row_ok = m < M;
+#pragma unroll
+      for (int j = 0; j < kColsPerThread; ++j) acc[j] = 0.f;
+      const float* bs_row = Bs + size_t(nt) * kblocks;
+      for (int kb = kb_begin; kb < kb_end; ++kb, ++acc_it) {
+        const int d = acc_it & 1;
+        const uint32_t dph = (acc_it >> 1) & 1u;
+        const float sa = row_ok ? __ldg(As + size_t(kb) * lds + m) : 0.f;
+        const float sb = __ldg(bs_row + kb);
+        // The decision must be warp-uniform: tcgen05.ld below is .sync.aligned.
+        const bool got = __all_sync(0xffffffffu, mbar_wait(&dfull[d], dph, abort_flag));
+        if (!got) {
+          raise_error(err, abort_flag, kSiteEpilogueFull);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t p[kColsPerThread];
+        const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(d * BN + half * kColsPerThread);
+        tmem_ld_x32(taddr, p);
+        tmem_ld_x32(taddr + 32, p + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[d]);
+        const float sc = sa * sb;
+#pragma unroll
+        for (int j = 0; j < kColsPerThread; ++j) acc[j] = fmaf(__uint_as_float(p[j]), sc, acc[j]);
+      }
+      if (ok && split == 1 && row_ok) {
+        store_row64(C + size_t(m) * ldc + size_t(nt) * BN + half * kColsPerThread, acc);
+      }
+    }
+  }
+
+  __syncwarp();   // single-lane roles rejoin their warp before the aligned barriers below
+  if (split > 1) {
+    // One tile per cluster: sum the ranks' accumulators through distributed
+    // shared memory, in rank order, into rank 0.  Every thread of every CTA
+    // reaches both cluster barriers, also after an abort.
+    const bool epi = warp >= 2;
+    const int m = last_mt * BM + row_in_tile;
+    const bool row_ok = epi && m < M;
+    float4* red = reinterpret_cast<float4*>(smem);   // [BN/4][BM] float4, reuses stages 0-1
+    if (row_ok && rank != 0) {
+#pragma unroll
+      for (int j4 = 0; j4 < kColsPerThread / 4; ++j4)
+        red[(half * (kColsPerThread / 4) + j4) * BM + row_in_tile] =
+            make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
+    }
+    cluster_sync();
+    if (row_ok && rank == 0) {
+      for (int r = 1; r < split; ++r) {
+        const uint32_t base = map_shared_rank(smem_u32(red), uint32_t(r));
+#pragma unroll
+        for (int j4 = 0; j4 < kColsPerThread / 4; ++j4) {
+          const float4 v =
+              ld_shared_cluster_f4(base + uint32_t(((half * (kColsPerThread / 4) + j4) * BM + row_in_tile) * 16));
+          acc[4 * j4] += v.x;
+          acc[4 * j4 + 1] += v.y;
+          acc[4 * j4 + 2] += v.z;
+          acc[4 * j4 + 3] += v.w;
+        }
+      }
+      if (!*abort_flag) store_row64(C + size_t(m) * ldc + size_t(last_nt) * BN + half * kColsPerThread, acc);
+    }
+    cluster_sync();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  static bool attr_done[64] = {};
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if (device < 64 && !attr_done[device]) {
+    e = cudaFuncSetAttribute(w8a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done[device] = true;
+  }
+  const int m_tiles = (p.M + BM - 1) / BM;
+  const int n_tiles = p.N / BN;
+  const int tiles = m_tiles * n_tiles;
+  const int kblocks = p.K / BK;
+  int split = 1;
+  if (tiles * 2 <= dev.num_sms) {
+    for (int s = kMaxSplitK; s >= 2; s >>= 1) {
+      if (tiles * s <= dev.num_sms && kblocks >= 2 * s) {
+        split = s;
+        break;
+      }
+    }
+  }
+  const int clusters = split > 1 ? tiles : (tiles < dev.num_sms ? tiles : dev.num_sms);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(clusters * split), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w8a8_kernel, p.tmA, p.tmB, p.As, p.lds, p.Bs,
+                            static_cast<__nv_bfloat16*>(p.C), p.ldc, p.M, p.N, p.K, split, p.err);
+}
+
+}  // namespace fp8blk

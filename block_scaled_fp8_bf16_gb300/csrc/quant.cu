@@ -1,0 +1,224 @@
+// Quantisers (bf16 -> e4m3 with fp32 block scales), the weight validator and
+// the decode diagnostic.
+//
+// Per-token activation quantisation ("Blockwise FP8 on Ada GPUs, part 2",
+// "The starting point": one scale per token per 128 values of K) follows the
+// warp-per-group shape the ArcKernels PR proposes in its "Route-2 handover"
+// (finding 3: one warp per 128-block, shuffle max reduction, vectorised
+// loads) instead of a 1024-thread block with 32 active threads: here each
+// warp takes two adjacent 128-groups of one row, sixteen lanes per group and
+// eight bf16 per lane (one 16-byte load), reduces |x| with four xor shuffles,
+// and writes eight codes per lane (one 8-byte store).  The pass reads 2 bytes
+// and writes 1 + 4/128 bytes per element and is bound by HBM bandwidth.
+//
+// The scale is s = amax / 448 with IEEE division, the codes are
+// e4m3(x / s) with IEEE division, round-to-nearest-even and saturation to
+// +-448 (cvt.rn.satfinite); amax == 0 gives s = 1.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "decode.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8blk {
+namespace {
+
+constexpr float kE4M3Max = 448.0f;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
+
+__device__ __forceinline__ float group_scale(float amax) {
+  return amax == 0.f ? 1.0f : __fdiv_rn(amax, kE4M3Max);
+}
+
+// One warp = two 128-groups (g0, g0+1) of one row.  Work items are ordered
+// row-fastest so that neighbouring warps write neighbouring scales.
+__global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
+                                                        int64_t ldx, uint8_t* __restrict__ a, int64_t lda,
+                                                        float* __restrict__ scales, int64_t lds) {
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;
+  const int hl = lane & 15;
+  const int64_t groups = K / 128;
+  const int64_t pairs = (groups + 1) / 2;
+  const int64_t items = M * pairs;
+  const int64_t warps_total = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < items; w += warps_total) {
+    const int64_t m = w % M;
+    const int64_t g = (w / M) * 2 + half;
+    const bool active = g < groups;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    const int64_t col = g * 128 + hl * 8;
+    if (active) v = ld_nc_v4(x + m * ldx + col);
+    float f[8];
+    bf16x8_to_f32(v, f);
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = group_scale(amax);
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(f[i], s);
+    if (active) {
+      uint2 out;
+      out.x = e4m3x4(q[0], q[1], q[2], q[3]);
+      out.y = e4m3x4(q[4], q[5], q[6], q[7]);
+      *reinterpret_cast<uint2*>(a + m * lda + col) = out;
+      if (hl == 0) scales[g * lds + m] = s;
+    }
+  }
+}
+
+// One CTA = one 128x128 weight block; 256 threads x 8 x (8 bf16).
+__global__ void __launch_bounds__(256) quant_weight_kernel(const __nv_bfloat16* __restrict__ w, int64_t N, int64_t K,
+                                                           int64_t ldw, uint8_t* __restrict__ b, int64_t ldb,
+                                                           float* __restrict__ scales) {
+  __shared__ float red[8];
+  const int64_t kb_count = K / 128;
+  const int64_t nb = blockIdx.x / kb_count;
+  const int64_t kb = blockIdx.x % kb_count;
+  const int tid = threadIdx.x;
+  uint4 v[8];
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = tid + 256 * j;      // 16-byte chunk index inside the block
+    const int r = i >> 4, c = i & 15;
+    v[j] = ld_nc_v4(w + (nb * 128 + r) * ldw + kb * 128 + c * 8);
+    float f[8];
+    bf16x8_to_f32(v[j], f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(f[t]));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const float s = group_scale(amax);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = tid + 256 * j;
+    const int r = i >> 4, c = i & 15;
+    float f[8];
+    bf16x8_to_f32(v[j], f);
+    uint2 out;
+    out.x = e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
+    out.y = e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+    *reinterpret_cast<uint2*>(b + (nb * 128 + r) * ldb + kb * 128 + c * 8) = out;
+  }
+  if (tid == 0) scales[nb * kb_count + kb] = s;
+}
+
+__global__ void validate_kernel(const uint8_t* __restrict__ b, int64_t ldb, const void* __restrict__ sc, int fmt,
+                                int64_t N, int64_t K, int32_t* __restrict__ counts) {
+  int nan_codes = 0, bad_scales = 0;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t chunks_per_row = K / 16;
+  for (int64_t i = tid; i < N * chunks_per_row; i += stride) {
+    const int64_t r = i / chunks_per_row, c = i % chunks_per_row;
+    const uint4 v = ld_nc_v4(b + r * ldb + c * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) nan_codes += ((w[j] >> (8 * t)) & 0x7Fu) == 0x7Fu;
+    }
+  }
+  if (fmt == 0) {
+    const float* s = static_cast<const float*>(sc);
+    for (int64_t i = tid; i < (N / 128) * (K / 128); i += stride) {
+      const float v = s[i];
+      bad_scales += !(isfinite(v) && v > 0.f);
+    }
+  } else {
+    const uint8_t* s = static_cast<const uint8_t*>(sc);
+    for (int64_t i = tid; i < (N / 32) * (K / 32); i += stride) {
+      const int e = int(s[i]) - 127;
+      bad_scales += (e < -14 || e > 7);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    nan_codes += __shfl_xor_sync(0xffffffffu, nan_codes, o);
+    bad_scales += __shfl_xor_sync(0xffffffffu, bad_scales, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    if (nan_codes) atomicAdd(&counts[0], nan_codes);
+    if (bad_scales) atomicAdd(&counts[1], bad_scales);
+  }
+}
+
+__global__ void debug_decode_kernel(const uint8_t* __restrict__ codes, int64_t n, int exp_shift,
+                                    uint32_t* __restrict__ out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;   // one word of 4 codes
+  if (i * 4 >= n) return;
+  const uint32_t q = *reinterpret_cast<const uint32_t*>(codes + 4 * i);
+  uint32_t lo, hi;
+  decode4_e4m3_bf16(q, decode_multiplier_bf16x2(exp_shift), lo, hi);
+  out[2 * i] = lo;
+  out[2 * i + 1] = hi;
+}
+
+int grid_for(int64_t items, int per_block, int num_sms, int waves) {
+  int64_t g = (items + per_block - 1) / per_block;
+  const int64_t cap = int64_t(num_sms) * waves;
+  if (g > cap) g = cap;
+  return g < 1 ? 1 : int(g);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const QuantActArgs& p, const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t items = p.M * ((p.K / 128 + 1) / 2);   // warps of work
+  const int grid = grid_for(items, 8, dev.num_sms, 16);
+  quant_act_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(p.x), p.M, p.K, p.ldx,
+                                        static_cast<uint8_t*>(p.a), p.lda, p.scales, p.lds);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight(const QuantWeightArgs& p, const DeviceInfo&, cudaStream_t s) {
+  const int64_t blocks = (p.N / 128) * (p.K / 128);
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  quant_weight_kernel<<<unsigned(blocks), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(p.w), p.N, p.K, p.ldw,
+                                                       static_cast<uint8_t*>(p.b), p.ldb, p.scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate(const ValidateArgs& p, const DeviceInfo& dev, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(p.counts, 0, 2 * sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
+  const int grid = grid_for(p.N * (p.K / 16), 256, dev.num_sms, 8);
+  validate_kernel<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(p.b), p.ldb, p.scales, p.fmt, p.N, p.K,
+                                       p.counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_decode(const void* codes, int64_t n, int exp_shift, void* out, cudaStream_t s) {
+  const int64_t words = n / 4;
+  const int grid = int((words + 255) / 256);
+  debug_decode_kernel<<<grid < 1 ? 1 : grid, 256, 0, s>>>(static_cast<const uint8_t*>(codes), n, exp_shift,
+                                                         static_cast<uint32_t*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace fp8blk

@@ -1,0 +1,243 @@
+/*
+ * fp8blk -- block-scaled FP8 linear layer for GB300 (sm_103a), C ABI.
+ *
+ * The layer computes, with FP32 accumulation and a bf16 result,
+ *
+ *     C[m, n] = sum_kb ( sum_{k in kb} A[m, k] * B[n, k] ) * As[kb, m] * Bs[n/128, kb]
+ *
+ * where kb runs over 128-wide blocks of K, B holds e4m3 weights with one fp32
+ * scale per 128x128 block, and A holds e4m3 activations with one fp32 scale
+ * per token per 128 values of K ("Blockwise FP8 on Ada GPUs, part 2",
+ * "The starting point" and "The fix").  The weight-only variant keeps the
+ * activations in bf16 ("perf(ArcKernels): blockwise-FP8 GEMM on tensor cores,
+ * scale promoted per 128-K", "What this adds"), and a second weight format
+ * stores one power-of-two UE8M0 scale per 32x32 block ("SM70 FP8 block-32
+ * kernels (PLI Labs)", "How it works").
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library never frees them and keeps no reference after the call.
+ *  - Matrices are row-major with an explicit leading dimension counted in
+ *    ELEMENTS (ld >= number of columns).
+ *  - Calls are asynchronous on the given stream (NULL = legacy default
+ *    stream) and return after the launch.  Argument errors are found on the
+ *    host before anything is launched; nothing is written in that case.
+ *  - No entry point allocates device memory on the compute path.  The only
+ *    host state is a small cache of TMA descriptors and per-device facts.
+ *  - e4m3 is the finite-only variant: 0x7F / 0xFF are NaN codes, max 448.
+ *  - Kernels never trap.  A pipeline wait that exceeds about one second
+ *    makes the kernel record FP8BLK_ERR_TIMEOUT in a per-device error word
+ *    and return; fp8blk_device_error() reads (and optionally clears) it.
+ *  - Every entry point is thread-safe with respect to the host cache.
+ *  - The library refuses to run on any device that is not compute
+ *    capability 10.3 (FP8BLK_ERR_ARCH).  There is no CPU fallback.
+ */
+#ifndef FP8BLK_H_
+#define FP8BLK_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8BLK_API __attribute__((visibility("default")))
+#else
+#define FP8BLK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* fp8blk_stream_t;
+
+typedef enum {
+  FP8BLK_OK = 0,
+  FP8BLK_ERR_INVALID_ARG = 1,       /* null pointer, negative size, ld < cols, lds < M */
+  FP8BLK_ERR_UNSUPPORTED_SHAPE = 2, /* N or K not a multiple of the scale block, M above a limit */
+  FP8BLK_ERR_MISALIGNED = 3,        /* pointer or row pitch not 16-byte aligned */
+  FP8BLK_ERR_ARCH = 4,              /* current device is not sm_103 */
+  FP8BLK_ERR_CUDA = 5,              /* a CUDA runtime/driver call or launch failed */
+  FP8BLK_ERR_NAN_CODE = 6,          /* fp8blk_validate_weights: an e4m3 NaN code was found */
+  FP8BLK_ERR_SCALE_WINDOW = 7,      /* fp8blk_validate_weights: a scale is out of range */
+  FP8BLK_ERR_TIMEOUT = 8            /* a kernel gave up on a pipeline wait (device error word) */
+} fp8blk_status;
+
+typedef enum {
+  /* fp32 scale per 128x128 weight block, array [N/128][K/128] row-major. */
+  FP8BLK_SCALE_F32_128x128 = 0,
+  /* one byte per 32x32 weight block, array [N/32][K/32] row-major; the byte
+   * holds 127 + e and the block's scale is 2^e, e in [-14, 7]. */
+  FP8BLK_SCALE_UE8M0_32x32 = 1
+} fp8blk_scale_fmt;
+
+/* Compile-time facts of the kernels, exported so that callers never
+ * duplicate them ("perf(ArcKernels) ...", "Correctness guards": eligibility
+ * is read from the kernel, not restated by the caller). */
+typedef struct {
+  int32_t abi_version;        /* FP8BLK_ABI_VERSION */
+  int32_t scale_block_k;      /* 128: K width of one fp32 scale block */
+  int32_t scale_block_n;      /* 128: N height of one fp32 weight scale block */
+  int32_t ue8m0_block;        /* 32: side of one UE8M0 block */
+  int32_t w8a8_tile_m;        /* rows of C per W8A8 tile */
+  int32_t w8a8_tile_n;        /* columns of C per W8A8 tile */
+  int32_t w8a16_tile_n;       /* weight rows per W8A16 tile */
+  int32_t w8a16_max_tile_m;   /* largest token tile of the W8A16 kernel */
+  int32_t gemv_max_m;         /* largest M accepted by fp8blk_gemv_w8a16 (16) */
+  int32_t ptr_align_bytes;    /* 16: required alignment of every tensor pointer */
+  int32_t row_align_bytes;    /* 16: required alignment of every row pitch */
+  int32_t lds_multiple;       /* 4: lds must be a multiple of this */
+  int32_t max_split_k;        /* largest split-K cluster the kernels use */
+} fp8blk_constraints;
+
+#define FP8BLK_ABI_VERSION 1
+
+/* ------------------------------------------------------------------------ */
+/* Hot path                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Per-token 1x128 activation quantisation to e4m3
+ * ("Blockwise FP8 on Ada GPUs, part 2", "The starting point";
+ *  "perf(ArcKernels) ...", "Route-2 handover", finding 2).
+ *
+ * For every row m and every group g of 128 consecutive K values:
+ *     amax = max |x[m, 128g .. 128g+127]|
+ *     s    = amax / 448 (IEEE float32 division); s = 1 when amax == 0
+ *     a[m, k] = e4m3(x[m, k] / s), round to nearest even, saturating to +-448
+ *     a_scales[g * lds + m] = s
+ *
+ *  x_bf16    [M, K] bf16, row pitch ldx elements (ldx*2 % 16 == 0).
+ *  a_e4m3    [M, K] e4m3 bytes out, row pitch lda bytes (lda % 16 == 0).
+ *  a_scales  [K/128][lds] float32 out; M is the contiguous axis
+ *            (the reading of "[M, ceil(K/128)], M-major"); lds >= M,
+ *            lds % 4 == 0.
+ *  K % 128 == 0.  M == 0 is a no-op.
+ *  Non-finite inputs are outside the contract.
+ */
+FP8BLK_API fp8blk_status fp8blk_quant_act(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                               void* a_e4m3, int64_t lda, float* a_scales, int64_t lds,
+                               fp8blk_stream_t stream);
+
+/*
+ * W8A8 block-scaled GEMM ("Blockwise FP8 on Ada GPUs, part 2", "The fix").
+ * For each 128-wide K block the kernel forms an FP32 partial on the tensor
+ * cores from e4m3 operands only, then promotes it once into the FP32
+ * accumulator, multiplied by As[kb, m] * Bs[n/128, kb].  C = bf16(acc),
+ * round to nearest even.
+ *
+ *  a_e4m3    [M, K] e4m3, row pitch lda bytes (lda % 16 == 0).
+ *  a_scales  [K/128][lds] float32 (as written by fp8blk_quant_act).
+ *  b_e4m3    [N, K] e4m3 weights, K contiguous, row pitch ldb bytes.
+ *  b_scales  [N/128][K/128] float32, row-major, packed.
+ *  c_bf16    [M, N] bf16 out, row pitch ldc elements (ldc*2 % 16 == 0).
+ *  N % 128 == 0, K % 128 == 0, M >= 0 (M == 0 is a no-op).
+ *  Weights are assumed finite (see fp8blk_validate_weights).
+ */
+FP8BLK_API fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda,
+                               const float* a_scales, int64_t lds,
+                               const void* b_e4m3, int64_t ldb,
+                               const float* b_scales,
+                               void* c_bf16, int64_t ldc,
+                               int64_t M, int64_t N, int64_t K,
+                               fp8blk_stream_t stream);
+
+/*
+ * W8A16 GEMM: bf16 activations, e4m3 weights decoded to bf16 in registers by
+ * integer operations, bf16 tensor-core products with FP32 accumulation
+ * ("FP8 / NVFP4 weight-only inference on the RTX 3090 loses nothing",
+ *  sections 2 and 4.1; "perf(ArcKernels) ...", "What this adds").
+ *
+ *  fmt == FP8BLK_SCALE_F32_128x128:
+ *     C[m, n] = sum_kb Bs[n/128, kb] * sum_{k in kb} x[m, k] * w[n, k],
+ *     one FP32 partial per 128-wide K block promoted with Bs.
+ *     b_scales: float32 [N/128][K/128].  N % 128 == 0, K % 128 == 0.
+ *  fmt == FP8BLK_SCALE_UE8M0_32x32 ("SM70 FP8 block-32 kernels", "Exactness"):
+ *     C[m, n] = sum_k x[m, k] * w[n, k] * 2^e[n/32, k/32],
+ *     the power of two is folded exactly into the decoded bf16 weight.
+ *     b_scales: uint8 [N/32][K/32] holding 127 + e.  N % 128 == 0, K % 128 == 0.
+ *
+ *  x_bf16  [M, K] bf16, row pitch ldx elements (ldx*2 % 16 == 0).
+ *  b_e4m3  [N, K] e4m3, row pitch ldb bytes (ldb % 16 == 0).
+ *  c_bf16  [M, N] bf16 out, row pitch ldc elements.
+ *  M == 0 is a no-op.  Scales outside [-14, 7] are outside the contract.
+ */
+FP8BLK_API fp8blk_status fp8blk_gemm_w8a16(const void* x_bf16, int64_t ldx,
+                                const void* b_e4m3, int64_t ldb,
+                                const void* b_scales, fp8blk_scale_fmt fmt,
+                                void* c_bf16, int64_t ldc,
+                                int64_t M, int64_t N, int64_t K,
+                                fp8blk_stream_t stream);
+
+/*
+ * Decode-size W8A16 product (M <= 16), same contract as fp8blk_gemm_w8a16.
+ * The weights are streamed once from HBM ("FP8 / NVFP4 weight-only
+ * inference ...", section 4.3: at small M the time is set by DRAM
+ * bandwidth).  M > 16 returns FP8BLK_ERR_UNSUPPORTED_SHAPE.
+ */
+FP8BLK_API fp8blk_status fp8blk_gemv_w8a16(const void* x_bf16, int64_t ldx,
+                                const void* b_e4m3, int64_t ldb,
+                                const void* b_scales, fp8blk_scale_fmt fmt,
+                                void* c_bf16, int64_t ldc,
+                                int64_t M, int64_t N, int64_t K,
+                                fp8blk_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Off the hot path                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * 128x128 block weight quantisation ("Blockwise FP8 on Ada GPUs, part 2",
+ * "The starting point"): the same rule as fp8blk_quant_act applied to each
+ * 128x128 block of w (amax over the block, s = amax / 448).
+ *
+ *  w_bf16    [N, K] bf16, row pitch ldw elements.
+ *  b_e4m3    [N, K] e4m3 out, row pitch ldb bytes.
+ *  b_scales  [N/128][K/128] float32 out, packed.
+ *  N % 128 == 0, K % 128 == 0.
+ */
+FP8BLK_API fp8blk_status fp8blk_quant_weight(const void* w_bf16, int64_t N, int64_t K, int64_t ldw,
+                                  void* b_e4m3, int64_t ldb, float* b_scales,
+                                  fp8blk_stream_t stream);
+
+/*
+ * Load-time weight check ("SM70 FP8 block-32 kernels", "Exactness": the
+ * packer refuses NaN codes and scales outside the window).
+ * Counts, on the device, into dev_counts[0] the e4m3 NaN codes of b and
+ * into dev_counts[1] the bad scales: for FP8BLK_SCALE_F32_128x128 a scale
+ * that is not finite or not > 0; for FP8BLK_SCALE_UE8M0_32x32 a byte whose
+ * exponent is outside [-14, 7].  dev_counts is a caller-owned device int32[2];
+ * it is overwritten.  Asynchronous: read dev_counts after the stream.
+ */
+FP8BLK_API fp8blk_status fp8blk_validate_weights(const void* b_e4m3, int64_t ldb,
+                                      const void* b_scales, fp8blk_scale_fmt fmt,
+                                      int64_t N, int64_t K, int32_t* dev_counts,
+                                      fp8blk_stream_t stream);
+
+/*
+ * Diagnostic: runs the W8A16 kernels' e4m3 -> bf16 integer decode on n codes
+ * and writes the bf16 bit patterns of dec(code) * 2^e, e = exp_shift in
+ * [-14, 7] (0 for the fp32-scale format).  codes: device uint8[n];
+ * out_bf16: device uint16[n].  n % 4 == 0.
+ */
+FP8BLK_API fp8blk_status fp8blk_debug_decode_e4m3(const void* codes, int64_t n, int32_t exp_shift,
+                                       void* out_bf16, fp8blk_stream_t stream);
+
+/* Fills *out with the kernels' compile-time constraints.  No device needed. */
+FP8BLK_API fp8blk_status fp8blk_query_constraints(fp8blk_constraints* out);
+
+/* Static English text for a status code.  Never NULL. */
+FP8BLK_API const char* fp8blk_status_string(fp8blk_status status);
+
+/*
+ * Reads the current device's error word (synchronises the device).
+ * *out_code receives the raw word (0 = no error; otherwise an internal code
+ * naming the wait that expired).  Returns FP8BLK_ERR_TIMEOUT when the word
+ * is set, FP8BLK_OK when clear.  clear != 0 resets the word to 0.
+ */
+FP8BLK_API fp8blk_status fp8blk_device_error(int32_t* out_code, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BLK_H_ */

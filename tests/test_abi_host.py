@@ -1,0 +1,142 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/fp8blk.h declares, and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8blk.h")
+
+
+@pytest.fixture(scope="module")
+def fp8blk():
+    from block_scaled_fp8_bf16_gb300 import build
+    build.build()
+    import block_scaled_fp8_bf16_gb300 as m
+    m._L()
+    return m
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"FP8BLK_API\s+[\w\s\*]+?\b(fp8blk_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for n in ("fp8blk_quant_act", "fp8blk_gemm_w8a8", "fp8blk_gemm_w8a16", "fp8blk_gemv_w8a16"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fp8blk):
+    lib = ctypes.CDLL(fp8blk.LIB_PATH)
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+    assert set(declared_symbols()) == set(fp8blk.EXPORTS)
+
+
+def test_no_other_dynamic_exports(fp8blk):
+    out = subprocess.run(["nm", "-D", "--defined-only", fp8blk.LIB_PATH], capture_output=True, text=True).stdout
+    ours = {l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("fp8blk")}
+    assert ours == set(declared_symbols())
+
+
+def test_no_cuda_driver_link_dependency(fp8blk):
+    out = subprocess.run(["ldd", fp8blk.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out and "libtorch" not in out
+
+
+def test_constraints(fp8blk):
+    c = fp8blk.fp8blk_query_constraints()
+    assert c["abi_version"] == 1
+    assert c["scale_block_k"] == 128 and c["scale_block_n"] == 128 and c["ue8m0_block"] == 32
+    assert c["gemv_max_m"] == 16 and c["ptr_align_bytes"] == 16 and c["lds_multiple"] == 4
+
+
+def test_status_strings(fp8blk):
+    for s in range(9):
+        assert len(fp8blk._L().fp8blk_status_string(s)) > 0
+    assert fp8blk._L().fp8blk_status_string(99) == b"unknown status"
+
+
+P = 1 << 20          # a 16-byte aligned fake pointer; never dereferenced
+MIS = P + 4          # misaligned fake pointer
+
+
+def call_w8a8(lib, a=P, lda=512, s=P, lds=16, b=P, ldb=512, bs=P, c=P, ldc=256, M=16, N=256, K=512):
+    return lib.fp8blk_gemm_w8a8(a, lda, s, lds, b, ldb, bs, c, ldc, M, N, K, None)
+
+
+def test_w8a8_argument_errors(fp8blk):
+    lib = fp8blk._L()
+    assert call_w8a8(lib, M=-1) == 1
+    assert call_w8a8(lib, N=200) == 2
+    assert call_w8a8(lib, K=500) == 2
+    assert call_w8a8(lib, M=0) == 0                 # no-op, no device needed
+    assert call_w8a8(lib, N=0) == 0
+    assert call_w8a8(lib, c=None) == 1
+    assert call_w8a8(lib, a=None) == 1
+    assert call_w8a8(lib, lda=256) == 1             # lda < K
+    assert call_w8a8(lib, lds=8) == 1               # lds < M
+    assert call_w8a8(lib, ldc=128) == 1             # ldc < N
+    assert call_w8a8(lib, a=MIS) == 3
+    assert call_w8a8(lib, bs=MIS) == 3
+    assert call_w8a8(lib, lda=520) == 3             # row pitch not 16 B
+    assert call_w8a8(lib, lds=18) == 3
+    assert call_w8a8(lib, ldc=260) == 3
+    assert call_w8a8(lib, M=1 << 31) == 2
+
+
+def test_w8a16_and_gemv_argument_errors(fp8blk):
+    lib = fp8blk._L()
+
+    def g(fn, x=P, ldx=512, b=P, ldb=512, sc=P, fmt=0, c=P, ldc=256, M=4, N=256, K=512):
+        return getattr(lib, fn)(x, ldx, b, ldb, sc, fmt, c, ldc, M, N, K, None)
+
+    for fn in ("fp8blk_gemm_w8a16", "fp8blk_gemv_w8a16"):
+        assert g(fn, fmt=2) == 1
+        assert g(fn, N=96) == 2
+        assert g(fn, K=96) == 2
+        assert g(fn, M=0) == 0
+        assert g(fn, sc=None) == 1
+        assert g(fn, ldx=256) == 1
+        assert g(fn, x=MIS) == 3
+        assert g(fn, ldx=516) == 3
+        assert g(fn, ldb=520) == 3
+    assert g("fp8blk_gemv_w8a16", M=17) == 2
+
+
+def test_quant_argument_errors(fp8blk):
+    lib = fp8blk._L()
+    q = lambda x=P, M=16, K=512, ldx=512, a=P, lda=512, s=P, lds=16: lib.fp8blk_quant_act(x, M, K, ldx, a, lda, s, lds, None)
+    assert q(M=-1) == 1
+    assert q(K=100) == 2
+    assert q(M=0) == 0
+    assert q(s=None) == 1
+    assert q(lds=15) == 1
+    assert q(lds=18) == 3
+    assert q(a=MIS) == 3
+    w = lambda N=256, K=512, ldw=512, ldb=512: lib.fp8blk_quant_weight(P, N, K, ldw, P, ldb, P, None)
+    assert w(N=100) == 2
+    assert w(ldw=100) == 1
+    v = lambda fmt=0, N=256, K=512, counts=P: lib.fp8blk_validate_weights(P, 512, P, fmt, N, K, counts, None)
+    assert v(fmt=3) == 1
+    assert v(counts=None) == 1
+    assert v(N=64) == 2
+    d = lambda n=256, e=0: lib.fp8blk_debug_decode_e4m3(P, n, e, P, None)
+    assert d(n=6) == 1
+    assert d(e=8) == 1
+    assert d(e=-15) == 1
+
+
+def test_valid_call_without_gpu_reports_cuda_or_arch(fp8blk):
+    """A well-formed call on a machine without an sm_103 device must fail
+    with a CUDA/arch status, never succeed silently."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call_w8a8(fp8blk._L()) in (4, 5)

@@ -1,0 +1,171 @@
+"""GPU parity of the W8A8 and W8A16 products against the float64 oracle,
+within |gpu - ref| <= 8e-3 |ref| + 2e-3 rms(ref row), elementwise."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from helpers import assert_gemm_close, bf16_out_to_f64, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def w8a8_inputs(seed, M, N, K, outliers=True):
+    x = synth.activations(seed, M, K, outliers=outliers)
+    a, As = O.quant_act_1x128(x)
+    b, Bs = O.quant_weight_128x128(synth.weights_bf16(seed, N, K))
+    return a, As, b, Bs
+
+
+def gpu_w8a8(a, As, b, Bs, ldc_pad=0, lds_pad=0):
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    M, K = a.shape
+    N = b.shape[0]
+    lds = fp8blk.act_scales_pitch(M) + lds_pad
+    s = np.zeros((K // 128, lds), dtype=np.float32)
+    s[:, :M] = As
+    c = torch.full((M, N + ldc_pad), 7.0, dtype=torch.bfloat16, device="cuda")
+    fp8blk.fp8blk_gemm_w8a8(to_dev(a), to_dev(s), to_dev(b), to_dev(Bs), c[:, :N])
+    torch.cuda.synchronize()
+    assert fp8blk.fp8blk_device_error() == 0
+    out = bf16_out_to_f64(c)
+    if ldc_pad:
+        assert np.all(out[:, N:] == 7.0)
+    return out[:, :N]
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (16, 256, 512),        # tiny workload
+    (1, 128, 128),         # single block, single row
+    (3, 256, 256),
+    (17, 384, 1024),
+    (129, 256, 2048),      # ragged second row tile
+    (255, 512, 512),
+    (128, 4096, 4096),     # split-K cluster path
+    (1, 4096, 4096),
+    (300, 1024, 1024),     # persistent path
+])
+def test_w8a8_matches_oracle(lib, M, N, K):
+    a, As, b, Bs = w8a8_inputs(M + N + K, M, N, K)
+    out = gpu_w8a8(a, As, b, Bs, ldc_pad=8 if M < 200 else 0, lds_pad=4)
+    assert_gemm_close(out, O.gemm_w8a8(a, As, b, Bs), f"w8a8 {M}x{N}x{K}")
+
+
+def test_w8a8_two_weight_scales_per_256_columns(lib):
+    """Neighbouring 128-column slices carry very different weight scales."""
+    M, N, K = 64, 512, 512
+    a, As, b, Bs = w8a8_inputs(9, M, N, K)
+    Bs = Bs * np.array([[1.0], [1000.0], [1e-3], [7.0]], dtype=np.float32)
+    assert_gemm_close(gpu_w8a8(a, As, b, Bs), O.gemm_w8a8(a, As, b, Bs), "w8a8 Bs slices")
+
+
+def test_w8a8_special_rows(lib):
+    """A zero row, an outlier row and a row of +-448 codes."""
+    M, N, K = 8, 256, 1024
+    x = synth.activations(3, M, K)
+    x[0] = 0
+    x[1, 5] = 0x4700          # 32768
+    x[2] = np.where(np.arange(K) % 2 == 0, 0x43E0, 0xC3E0)   # +-448
+    a, As = O.quant_act_1x128(x)
+    b, Bs = O.quant_weight_128x128(synth.weights_bf16(3, N, K))
+    out = gpu_w8a8(a, As, b, Bs)
+    ref = O.gemm_w8a8(a, As, b, Bs)
+    assert np.all(out[0] == 0)
+    assert_gemm_close(out, ref, "w8a8 special rows")
+
+
+def test_w8a8_full_size_sampled_rows(lib):
+    """o_proj shape at M = 4096 in the benchmark's launch configuration,
+    checked on 64 sampled rows."""
+    M, N, K = 4096, 4096, 4096
+    a, As, b, Bs = w8a8_inputs(0, M, N, K)
+    out = gpu_w8a8(a, As, b, Bs)
+    rows = synth.sample_rows(0, M, 64)
+    assert_gemm_close(out[rows], O.gemm_w8a8_rows(a, As, b, Bs, rows), "w8a8 4096^3 sampled")
+
+
+def test_w8a8_one_hot_rows(lib):
+    """Each A row holds a single 1.0 at column k0: C row = Bs * dec(B[:, k0])."""
+    N, K = 256, 512
+    ks = [0, 31, 32, 127, 128, 300, 511]
+    a = np.zeros((len(ks), K), dtype=np.uint8)
+    for i, k0 in enumerate(ks):
+        a[i, k0] = 0x38
+    As = np.ones((K // 128, len(ks)), dtype=np.float32)
+    b, Bs = O.quant_weight_128x128(synth.weights_bf16(4, N, K))
+    out = gpu_w8a8(a, As, b, Bs)
+    ref = O.gemm_w8a8(a, As, b, Bs)
+    assert np.array_equal(out, O.bf16_bits_to_f64(O.f64_to_bf16_bits(ref)))
+
+
+def gpu_w8a16(x, b, sc, fmt, gemv=False, ldx_pad=0):
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    M, K = x.shape
+    N = b.shape[0]
+    xf = np.zeros((M, K + ldx_pad), dtype=np.uint16)
+    xf[:, :K] = x
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    fn = fp8blk.fp8blk_gemv_w8a16 if gemv else fp8blk.fp8blk_gemm_w8a16
+    fn(to_dev_bf16(xf)[:, :K], to_dev(b), to_dev(sc), fmt, c)
+    torch.cuda.synchronize()
+    assert fp8blk.fp8blk_device_error() == 0
+    return bf16_out_to_f64(c)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (2, 256, 512), (4, 384, 1024), (8, 512, 384),
+                                   (16, 256, 14336), (5, 28672, 256)])
+def test_gemv_w8a16_f32(lib, M, N, K):
+    x = synth.activations(M + K, M, K)
+    b, Bs = O.quant_weight_128x128(synth.weights_bf16(M + N, N, K))
+    out = gpu_w8a16(x, b, Bs, 0, gemv=True, ldx_pad=8)
+    assert_gemm_close(out, O.gemm_w8a16_f32scale(x, b, Bs), f"gemv f32 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 2048, 7168), (4, 7168, 2048), (16, 256, 512), (3, 128, 128)])
+def test_gemv_w8a16_ue8m0(lib, M, N, K):
+    x = synth.activations(M, M, K)
+    b, e = synth.ue8m0_weights(N, N, K)
+    out = gpu_w8a16(x, b, e, 1, gemv=True)
+    assert_gemm_close(out, O.gemm_w8a16_ue8m0(x, b, e), f"gemv ue8m0 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 256, 512), (32, 512, 1024), (33, 256, 256), (64, 384, 2048),
+                                   (100, 256, 512), (128, 512, 512), (129, 256, 1024), (512, 1024, 512)])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_gemm_w8a16(lib, M, N, K, fmt):
+    x = synth.activations(M * 3 + K, M, K, outliers=True)
+    if fmt == 0:
+        b, sc = O.quant_weight_128x128(synth.weights_bf16(N, N, K))
+        ref = O.gemm_w8a16_f32scale(x, b, sc)
+    else:
+        b, sc = synth.ue8m0_weights(N + K, N, K)
+        ref = O.gemm_w8a16_ue8m0(x, b, sc)
+    out = gpu_w8a16(x, b, sc, fmt)
+    assert_gemm_close(out, ref, f"w8a16 fmt{fmt} {M}x{N}x{K}")
+
+
+def test_w8a16_ue8m0_full_size_sampled(lib):
+    M, N, K = 4096, 7168, 2048
+    x = synth.activations(1, M, K)
+    b, e = synth.ue8m0_weights(1, N, K)
+    out = gpu_w8a16(x, b, e, 1)
+    rows = synth.sample_rows(1, M, 32)
+    assert_gemm_close(out[rows], O.gemm_w8a16_ue8m0_rows(x, b, e, rows), "w8a16 ue8m0 4096 sampled")
+
+
+def test_w8a16_one_hot_columns_exact_decode(lib):
+    """x rows with a single 1.0 read one weight column through the bf16 MMA:
+    every finite code must come back exactly times its block scale."""
+    N, K = 256, 256
+    b = np.zeros((N, K), dtype=np.uint8)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    b[:254, 0] = finite
+    b[:254, 200] = finite[::-1]
+    e = synth.ue8m0_scale_bytes(5, (N // 32, K // 32))
+    x = np.zeros((2, K), dtype=np.uint16)
+    x[0, 0] = 0x3F80
+    x[1, 200] = 0x3F80
+    out = gpu_w8a16(x, b, e, 1)
+    ref = O.gemm_w8a16_ue8m0(x, b, e)
+    assert np.array_equal(out, ref)          # exact: a single product, no rounding

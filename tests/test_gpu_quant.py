@@ -1,0 +1,112 @@
+"""GPU parity of the quantisers and the decode: bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from helpers import groups_with_amax, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_quant_act(x_bits, lds_pad=0, ldx_pad=0):
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    M, K = x_bits.shape
+    xfull = np.zeros((M, K + ldx_pad), dtype=np.uint16)
+    xfull[:, :K] = x_bits
+    xt = to_dev_bf16(xfull)[:, :K]
+    a = torch.full((M, K), 0xAB, dtype=torch.uint8, device="cuda")
+    lds = fp8blk.act_scales_pitch(M) + lds_pad
+    s = torch.full((K // 128, lds), -7.0, dtype=torch.float32, device="cuda")
+    fp8blk.fp8blk_quant_act(xt, a, s)
+    torch.cuda.synchronize()
+    return a.cpu().numpy(), s.cpu().numpy(), lds
+
+
+@pytest.mark.parametrize("M,K,outliers", [(16, 512, False), (1, 128, False), (3, 384, True), (17, 1024, True),
+                                          (129, 4096, True), (300, 256, False)])
+def test_quant_act_matches_oracle(lib, M, K, outliers):
+    x = synth.activations(M * 7 + K, M, K, outliers=outliers)
+    a, s, lds = gpu_quant_act(x, lds_pad=4, ldx_pad=64)
+    qa, qs = O.quant_act_1x128(x)
+    assert np.array_equal(a, qa)
+    assert np.array_equal(s[:, :M].view(np.uint32), qs.view(np.uint32))
+    assert np.all(s[:, M:] == -7.0)            # padding of the scale pitch untouched
+
+
+@pytest.mark.parametrize("amax_bits", [0x3F80, 0x43E0, 0x40F0, 0x7F7F, 0x0080, 0x0003])
+def test_quant_act_exhaustive_bf16_groups(lib, amax_bits):
+    rng = np.random.default_rng(5)
+    g = groups_with_amax(amax_bits, rng)                 # [n, 128]
+    if g.shape[0] % 2:
+        g = np.concatenate([g, g[-1:]], axis=0)
+    x = g.reshape(g.shape[0] // 2, 256)                  # two groups per row
+    a, s, _ = gpu_quant_act(x)
+    qa, qs = O.quant_act_1x128(x)
+    assert np.array_equal(a, qa)
+    assert np.array_equal(s[:, : x.shape[0]].view(np.uint32), qs.view(np.uint32))
+
+
+def test_quant_act_zero_and_signed_zero_groups(lib):
+    x = np.zeros((4, 256), dtype=np.uint16)
+    x[1, :128] = 0x8000
+    x[2, 5] = 0x3F80
+    x[3] = 0x8000
+    a, s, _ = gpu_quant_act(x)
+    qa, qs = O.quant_act_1x128(x)
+    assert np.array_equal(a, qa)
+    assert np.array_equal(s[:, :4], qs)
+
+
+def test_quant_act_large_row_count_sampled(lib):
+    M, K = 8192, 7168
+    x = synth.activations(0, M, K)
+    a, s, _ = gpu_quant_act(x)
+    rows = synth.sample_rows(0, M, 64)
+    qa, qs = O.quant_act_1x128(x[rows])
+    assert np.array_equal(a[rows], qa)
+    assert np.array_equal(s[:, rows], qs)
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 512), (384, 1024)])
+def test_quant_weight_matches_oracle(lib, N, K):
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    w = synth.weights_bf16(N + K, N, K)
+    b, bs = fp8blk.quant_weight(to_dev_bf16(w))
+    torch.cuda.synchronize()
+    qb, qbs = O.quant_weight_128x128(w)
+    assert np.array_equal(b.cpu().numpy(), qb)
+    assert np.array_equal(bs.cpu().numpy().view(np.uint32), qbs.view(np.uint32))
+
+
+@pytest.mark.parametrize("e", [0, -14, -1, 3, 7])
+def test_decode_all_codes_exact(lib, e):
+    """The kernels' integer e4m3 -> bf16 decode gives dec(code) * 2^e exactly,
+    for every finite code including subnormals and both zeros."""
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F] + [0, 0], dtype=np.uint8)   # 256 = 4k
+    ct = to_dev(codes)
+    out = torch.zeros(codes.size, dtype=torch.int16, device="cuda")
+    fp8blk.fp8blk_debug_decode_e4m3(ct, e, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint16)
+    ref = O.f64_to_bf16_bits(O.e4m3_decode(codes) * 2.0 ** e)
+    assert np.array_equal(got, ref)
+
+
+def test_validate_weights_counts(lib):
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    b = synth.finite_e4m3_codes(1, (256, 512))
+    b[3, 7] = 0x7F
+    b[200, 511] = 0xFF
+    bs = np.full((2, 4), 0.01, dtype=np.float32)
+    bs[1, 2] = np.inf
+    bs[0, 0] = 0.0
+    assert fp8blk.validate_weights(to_dev(b), to_dev(bs), fp8blk.SCALE_F32_128x128) == (2, 2)
+    e = np.full((8, 16), 127, dtype=np.uint8)
+    e[0, 0] = 127 - 15
+    e[7, 15] = 127 + 8
+    e[3, 3] = 127 + 7
+    b2 = synth.finite_e4m3_codes(2, (256, 512))
+    assert fp8blk.validate_weights(to_dev(b2), to_dev(e), fp8blk.SCALE_UE8M0_32x32) == (0, 2)
