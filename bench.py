@@ -1,0 +1,549 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled FP8 linear layer on GB300.
+
+Headline step (one pass of the W8A8 hot path over one batch): per-token 1x128
+activation quantisation + block-scaled W8A8 GEMM for the o_proj shape
+N = K = 4096 at M = 4096 tokens, with inputs resident in HBM.  Inputs and
+weights are rotated over enough copies that every step reads them from HBM
+(the rotated set is larger than twice the L2 cache).
+
+One JSON line on stdout (rank 0).  `--sweep` additionally times every
+workload shape (W8A8 o_proj / prefill, W8A16 decode and UE8M0) with CUDA-graph
+replays over rotated weights and writes a table to gpurun_out/sweep.json.
+
+`--impl reference` times the float64 CPU oracle on a bounded row sample of the
+same workload (the oracle is the only reference implementation there is).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+# The CPU oracle uses numpy's BLAS; pin its thread count to the cores we have
+# so the reported core count is the one used.
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+METRIC = "block-FP8 GEMM TFLOP/s (M≥256), weight GB/s (M≤16); % of GB300 roofline"
+HEAD_M, HEAD_N, HEAD_K = 4096, 4096, 4096
+WORKLOAD = "W8A8 o_proj linear, N=K=4096, M=4096: act quant (1x128) + block-scaled GEMM"
+FP8_PER_BF16 = 2.0       # nominal dense fp8 : bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+
+def peaks():
+    p = {}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+    if "hbm_gbs" in p and "bf16_tflops" in p:
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"],
+                "bf16_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling in the background; each line is stamped with the
+    host time it arrived so that only samples inside the timed region count."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.dev = device_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        import threading
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append((time.perf_counter(), line))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        time.sleep(0.5)
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(2 * self.period / 1000.0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        window = [l for t, l in self.lines if self.t0 is not None and self.t0 <= t <= (self.t1 or t)]
+        if not window:     # region shorter than one sampling period: take the first sample after it began
+            window = [l for t, l in self.lines if self.t0 is not None and t >= self.t0][:1]
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in window:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="gloo")
+    return world, rank, local
+
+
+def dist_max(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)])
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def _rot_copies(bytes_per_copy: int, l2_bytes: int, cap: int = 64) -> int:
+    need = 2 * l2_bytes
+    return max(2, min(cap, -(-need // max(1, bytes_per_copy))))
+
+
+def build_w8a8_set(M, N, K, copies, seed=0, outliers=True):
+    import torch
+
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    from synth import torch_gen as tg
+    x0 = tg.activations(seed, M, K, outliers=outliers)
+    w0 = tg.weights_bf16(seed, N, K)
+    b0, bs0 = fp8blk.quant_weight(w0)
+    del w0
+    sets = []
+    lds = fp8blk.act_scales_pitch(M)
+    for _ in range(copies):
+        sets.append({
+            "x": x0.clone(), "b": b0.clone(), "bs": bs0.clone(),
+            "a": torch.empty((M, K), dtype=torch.uint8, device="cuda"),
+            "s": torch.empty((K // 128, lds), dtype=torch.float32, device="cuda"),
+            "c": torch.empty((M, N), dtype=torch.bfloat16, device="cuda"),
+        })
+    return sets
+
+
+def gpu_arm(args, world, rank, local):
+    import torch
+
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    torch.cuda.set_device(local)
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    M, N, K = HEAD_M, HEAD_N, HEAD_K
+    per_copy = M * K * 2 + M * K + N * K + M * N * 2 + (K // 128) * M * 4
+    R = _rot_copies(per_copy, l2)
+    sets = build_w8a8_set(M, N, K, R)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s = sets[i % R]
+        fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"], stream)
+        fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"], stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if fp8blk.fp8blk_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # Timed region: K steps, events around the whole region and around every
+    # GEMM launch (the dominant kernel), all on the launching stream.
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    clocks.mark_start()
+    ev0.record(stream)
+    for i in range(args.steps):
+        s = sets[i % R]
+        fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"], stream)
+        g0[i].record(stream)
+        fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"], stream)
+        g1[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    clk = clocks.stop()
+    dist_barrier(world)
+    ms_total = dist_max(ev0.elapsed_time(ev1), world)
+    gemm_ms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / args.steps
+    err = fp8blk.fp8blk_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed region")
+
+    flop = 2.0 * M * N * K
+    ms_step = ms_total / args.steps
+    value = world * flop / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    fp8_peak = pk["bf16"] * FP8_PER_BF16
+    achieved = flop / (gemm_ms * 1e-3) / 1e12
+
+    # End to end through the C ABI from pinned host buffers: H2D of x, quant,
+    # GEMM, D2H of C, every step, inside the timed region.
+    e2e_steps = max(3, min(args.steps, 100))
+    xh = [sets[i]["x"].cpu().pin_memory() for i in range(R)]
+    ch = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    for i in range(2):
+        s = sets[i % R]
+        s["x"].copy_(xh[i % R], non_blocking=True)
+        step(i)
+        ch.copy_(s["c"], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        s = sets[i % R]
+        s["x"].copy_(xh[i % R], non_blocking=True)
+        fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"], stream)
+        fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"], stream)
+        ch.copy_(s["c"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1), world) / e2e_steps
+    e2e_value = world * flop / (e2e_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 (bf16 in/out)",
+        "data": "synthetic (seeded torch generators: x ~ N(0,1) with 1% outlier channels x20, w ~ N(0,0.02))",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K,
+                   "l2": f"inputs rotated over {R} copies ({R * per_copy / 2**20:.0f} MiB > 2x L2 {l2 / 2**20:.0f} MiB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "w8a8_kernel (block-scaled e4m3 GEMM)",
+                     "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / fp8_peak, 4),
+                     "peak_note": f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x {FP8_PER_BF16} (nominal fp8:bf16)",
+                     "gemm_us": round(gemm_ms * 1e3, 2), "traffic": None},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2, "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    return line
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_linear_sample(rows: int, seed: int = 0):
+    """Inputs for the oracle leg: the same workload (N = K = 4096) on a seeded
+    row sample.  Weight quantisation is input preparation, not timed."""
+    import numpy as np
+
+    import oracle
+    import synth
+    x = synth.activations(seed, HEAD_M, HEAD_K, outliers=True)
+    idx = synth.sample_rows(seed, HEAD_M, rows)
+    b, bs = oracle.quant_weight_128x128(synth.weights_bf16(seed, HEAD_N, HEAD_K))
+    return np.ascontiguousarray(x[idx]), b, bs
+
+
+def oracle_step(xs, b, bs):
+    import oracle
+    a, s = oracle.quant_act_1x128(xs)
+    return oracle.gemm_w8a8(a, s, b, bs)
+
+
+def cpu_baseline(rows: int = 64, min_seconds: float = 10.0):
+    xs, b, bs = oracle_linear_sample(rows)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_step(xs, b, bs)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or n >= 200:
+            break
+    per = dt / n
+    value = 2.0 * rows * HEAD_N * HEAD_K / per / 1e12
+    return {"value": round(value, 6), "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
+            "sample": f"{rows} seeded rows of the M=4096 o_proj batch (N=K=4096), act quant + W8A8 product in "
+                      f"float64 numpy, {n} repetitions over {dt:.1f} s"}
+
+
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return None
+    rows = 64
+    xs, b, bs = oracle_linear_sample(rows)
+    for _ in range(args.warmup):
+        oracle_step(xs, b, bs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(xs, b, bs)
+    dt = time.perf_counter() - t0
+    per = dt / args.steps
+    value = 2.0 * rows * HEAD_N * HEAD_K / per / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy generators)",
+        "config": {"workload": WORKLOAD, "M": HEAD_M, "N": HEAD_N, "K": HEAD_K,
+                   "sample": f"{rows} rows per step", "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
+                         "sample": f"{rows} seeded rows of the M=4096 batch per step"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------- sweep
+
+def sweep(out_path):
+    """Times every workload shape with CUDA-graph replays over rotated copies."""
+    import torch
+
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    from synth import torch_gen as tg
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    pk = peaks()
+    rows = []
+
+    def graph_time(calls, reps=10):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for c in calls:
+                c()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in calls:
+                c()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / len(calls))
+        if fp8blk.fp8blk_device_error() != 0:
+            raise RuntimeError("device error word set")
+        return statistics.median(times) * 1e3     # us per call
+
+    def record(kind, M, N, K, us, flop, bytes_, tensor_peak):
+        t_tensor = flop / (tensor_peak * 1e12)
+        t_hbm = bytes_ / (pk["hbm_gbs"] * 1e9)
+        roof_us = max(t_tensor, t_hbm) * 1e6
+        rows.append({"kind": kind, "M": M, "N": N, "K": K, "us": round(us, 3),
+                     "tflops": round(flop / (us * 1e-6) / 1e12, 2),
+                     "weight_gbs": round(N * K / (us * 1e-6) / 1e9, 1),
+                     "bytes_gbs": round(bytes_ / (us * 1e-6) / 1e9, 1),
+                     "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+                     "roofline_frac": round(roof_us / us, 4)})
+        print(json.dumps(rows[-1]), file=sys.stderr)
+
+    fp8_peak = pk["bf16"] * FP8_PER_BF16
+    # W8A8: o_proj and prefill shapes (GEMM alone, and quant+GEMM)
+    w8a8 = [(M, 4096, 4096) for M in (1, 16, 128, 1024, 4096)] + [(16, 256, 512)]
+    for M in (256, 2048, 8192):
+        for N, K in ((7168, 2048), (2048, 7168), (18432, 7168), (7168, 18432)):
+            w8a8.append((M, N, K))
+    for M, N, K in w8a8:
+        per = M * K * 3 + N * K + M * N * 2
+        R = _rot_copies(per, l2, cap=32)
+        sets = build_w8a8_set(M, N, K, R, outliers=(N == 4096 and K == 4096))
+        calls = [lambda s=s: fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"]) for s in sets]
+        for s in sets:
+            fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"])
+        byt = M * K + (K // 128) * M * 4 + N * K + (N // 128) * (K // 128) * 4 + 2 * M * N
+        record("w8a8_gemm", M, N, K, graph_time(calls), 2.0 * M * N * K, byt, fp8_peak)
+        calls2 = [lambda s=s: (fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"]),
+                               fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"])) for s in sets]
+        record("w8a8_linear", M, N, K, graph_time(calls2), 2.0 * M * N * K, byt + 2 * M * K, fp8_peak)
+        qcalls = [lambda s=s: fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"]) for s in sets]
+        record("quant_act", M, 0, K, graph_time(qcalls), 0.0, 3 * M * K + (K // 128) * M * 4, fp8_peak)
+        del sets
+        torch.cuda.empty_cache()
+    # W8A16 fp32-scale decode and UE8M0
+    w8a16 = []
+    for N, K in ((4096, 4096), (28672, 4096), (4096, 14336)):
+        for M in (1, 2, 4, 8, 16):
+            w8a16.append((0, M, N, K))
+    for N, K in ((2048, 7168), (7168, 2048)):
+        for M in (1, 4, 16, 32, 128, 512, 4096):
+            w8a16.append((1, M, N, K))
+    for fmt, M, N, K in w8a16:
+        per = N * K + M * K * 2 + M * N * 2
+        R = _rot_copies(per, l2, cap=64)
+        x = tg.activations(1, M, K)
+        if fmt == 0:
+            b, bs = fp8blk.quant_weight(tg.weights_bf16(1, N, K))
+        else:
+            b, bs = tg.ue8m0_weights(1, N, K)
+        sets = [(x.clone(), b.clone(), bs.clone(), torch.empty((M, N), dtype=torch.bfloat16, device="cuda"))
+                for _ in range(R)]
+        fn = fp8blk.fp8blk_gemv_w8a16 if M <= 16 else fp8blk.fp8blk_gemm_w8a16
+        calls = [lambda s=s: fn(s[0], s[1], s[2], fmt, s[3]) for s in sets]
+        sc_bytes = (N // 128) * (K // 128) * 4 if fmt == 0 else (N // 32) * (K // 32)
+        byt = N * K + sc_bytes + M * K * 2 + M * N * 2
+        record("w8a16_f32" if fmt == 0 else "w8a16_ue8m0", M, N, K, graph_time(calls), 2.0 * M * N * K, byt,
+               pk["bf16"])
+        del sets
+        torch.cuda.empty_cache()
+    with open(out_path, "w") as f:
+        json.dump({"peaks": pk, "fp8_peak": fp8_peak, "rows": rows}, f, indent=1)
+
+
+# ---------------------------------------------------------------- profiling cases
+
+def run_case(spec: str, iters: int):
+    """Runs one kernel configuration `iters` times, untimed (for ncu captures).
+    spec: w8a8:M,N,K | quant:M,K | w8a16:M,N,K,fmt"""
+    import torch
+
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    from synth import torch_gen as tg
+    kind, dims = spec.split(":")
+    v = [int(t) for t in dims.split(",")]
+    if kind in ("w8a8", "quant"):
+        if kind == "w8a8":
+            M, N, K = v
+        else:
+            (M, K), N = v, 128
+        s = build_w8a8_set(M, N, K, 1)[0]
+        for _ in range(iters):
+            fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"])
+            if kind == "w8a8":
+                fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"])
+    elif kind == "w8a16":
+        M, N, K, fmt = v
+        x = tg.activations(1, M, K)
+        if fmt == 0:
+            b, bs = fp8blk.quant_weight(tg.weights_bf16(1, N, K))
+        else:
+            b, bs = tg.ue8m0_weights(1, N, K)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        for _ in range(iters):
+            fp8blk.fp8blk_gemm_w8a16(x, b, bs, fmt, c)
+    else:
+        raise SystemExit(f"unknown case {spec}")
+    torch.cuda.synchronize()
+    if fp8blk.fp8blk_device_error() != 0:
+        raise SystemExit("device error word set")
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--sweep", action="store_true", help="also time every workload shape")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None, help="run one configuration untimed (w8a8:M,N,K | quant:M,K | "
+                                                  "w8a16:M,N,K,fmt) for profiling")
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args()
+    if args.case:
+        import block_scaled_fp8_bf16_gb300 as fp8blk
+        fp8blk._L()
+        run_case(args.case, args.iters)
+        return
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        line = reference_arm(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    fp8blk._L()
+    line = gpu_arm(args, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline()
+        if args.sweep:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            sweep(os.path.join(ROOT, "gpurun_out", "sweep.json"))
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
