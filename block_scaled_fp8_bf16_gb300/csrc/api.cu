@@ -84,6 +84,7 @@ struct MapKey {
   const void* ptr;
   uint64_t inner, outer, stride_bytes;
   uint32_t box_inner, box_outer;
+  int swizzle;
   bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 
@@ -98,9 +99,9 @@ MapEntry g_cache[kCacheSize];
 int g_cache_next = 0;
 std::mutex g_cache_mu;
 
-// 2-D tiled map, 128-byte swizzle, zero fill outside the tensor.
+// 2-D tiled map, zero fill outside the tensor; 128-byte swizzle unless told otherwise.
 fp8blk_status make_map(CUtensorMap& out, CUtensorMapDataType dtype, const void* ptr, uint64_t inner, uint64_t outer,
-                       uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+                       uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128 = true) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FP8BLK_ERR_CUDA;
   MapKey key;
@@ -113,6 +114,7 @@ fp8blk_status make_map(CUtensorMap& out, CUtensorMapDataType dtype, const void* 
   key.stride_bytes = stride_bytes;
   key.box_inner = box_inner;
   key.box_outer = box_outer;
+  key.swizzle = swizzle128 ? 1 : 0;
   {
     std::lock_guard<std::mutex> lk(g_cache_mu);
     for (int i = 0; i < kCacheSize; ++i) {
@@ -130,7 +132,8 @@ fp8blk_status make_map(CUtensorMap& out, CUtensorMapDataType dtype, const void* 
   const cuuint32_t estr[2] = {1, 1};
   CUtensorMap m;
   const CUresult r = fn(&m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return FP8BLK_ERR_CUDA;
   {
@@ -245,8 +248,11 @@ fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda, const float* a_s
   st = make_map(p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_e4m3, uint64_t(K), uint64_t(N), uint64_t(ldb), 128,
                 kW8A8TileN);
   if (st != FP8BLK_OK) return st;
-  p.As = a_scales;
-  p.lds = lds;
+  // Scales are read through the full pitch (lds >= M, a multiple of 4, so
+  // 16-byte rows); rows past M are never stored.
+  st = make_map(p.tmAs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scales, uint64_t(lds), uint64_t(K / 128),
+                uint64_t(lds) * 4, kW8A8TileM, 1, false);
+  if (st != FP8BLK_OK) return st;
   p.Bs = b_scales;
   p.C = c_bf16;
   p.ldc = ldc;

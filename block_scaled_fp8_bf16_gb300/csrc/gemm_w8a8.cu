@@ -9,16 +9,20 @@
 // As * Bs.  On sm_103a the partial lives in tensor memory (TMEM), so the
 // per-slice fragments that spilled registers on Ada never exist here:
 //
-//   warp 0      TMA producer: A tile [128 x 128 B] and B tile [128 x 128 B]
-//               per 128-K block into a 6-stage shared-memory ring.
-//   warp 1      allocates 256 TMEM columns; one thread issues four
+//   warp 0      TMA producer: A tile [128 x 128 B], B tile [128 x 128 B] and
+//               the tile rows' activation scales As[kb, m0..m0+127] per 128-K
+//               block into a 6-stage shared-memory ring.
+//   warp 1      allocates all 512 TMEM columns; one thread issues four
 //               tcgen05.mma kind::f8f6f4 (K = 32 each) per K block into one
-//               of two 128-column partial buffers (double buffered, so the
-//               next block's MMA overlaps this block's promotion).
+//               of four 128-column partial buffers, so the tensor cores run up
+//               to three K blocks ahead of the promotion.
 //   warps 2..9  promotion + epilogue: each thread owns one row and 64
 //               columns of the 128x128 tile; per K block it reads its partial
 //               with tcgen05.ld, releases the buffer, and does
 //               acc = fma(partial, As[kb, m] * Bs[n/128, kb], acc).
+//               Activation scales come from shared memory (loaded by TMA with
+//               the operands), weight scales from a per-lane register window
+//               handed out by shuffle, so no global load sits on this path.
 //               At the end of the tile it rounds to bf16 and stores C.
 //
 // The weight scale is looked up per 128-wide N slice of the tile, never once
@@ -48,20 +52,23 @@ constexpr int kStages = 6;
 constexpr int kStageA = BM * BK;
 constexpr int kStageB = BN * BK;
 constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kStageAs = BM * 4;          // fp32 activation scales of the tile's rows for one K block
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kColsPerThread = BN / 2;   // two epilogue warps share a TMEM lane quarter
-constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kAccBufs = 4;              // FP32 partials in flight in TMEM
+constexpr uint32_t kTmemCols = kAccBufs * BN;
 constexpr uint32_t kIdesc = make_idesc(0 /* e4m3 */, BM, BN);
 constexpr int kGroupM = 8;
-constexpr int kBarrierBytes = 256;
-constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + kBarrierBytes + 1024;
+constexpr int kBarrierBytes = 512;
+constexpr size_t kSmemBytes = size_t(kStages) * (kStageBytes + kStageAs) + kBarrierBytes + 1024;
 
 static_assert(BK == 128, "one MMA K block must be exactly one scale block");
 static_assert(kTmemCols <= 512, "TMEM budget");
 static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 N for M = 128");
 static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "128B-swizzle atoms need 1024-B alignment");
 static_assert(2 * kStageBytes >= BM * BN * 4, "split-K reduction buffer reuses two stages");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mt, int& nt) {
   const int per_group = kGroupM * n_tiles;
@@ -93,17 +100,18 @@ __device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* acc
 
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const float* __restrict__ As, int64_t lds, const float* __restrict__ Bs,
+                const __grid_constant__ CUtensorMap tmAs, const float* __restrict__ Bs,
                 __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N, int K, int split,
                 int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes);
+  float* as_stage = reinterpret_cast<float*>(smem + size_t(kStages) * kStageBytes);   // [kStages][BM]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * (kStageBytes + kStageAs));
   uint64_t* empty = full + kStages;
   uint64_t* dfull = empty + kStages;
-  uint64_t* dempty = dfull + 2;
-  uint64_t* drain = dempty + 2;
+  uint64_t* dempty = dfull + kAccBufs;
+  uint64_t* drain = dempty + kAccBufs;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -122,9 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 1 + kEpiWarps);   // MMA done with A/B, epilogue done with the scales
     }
-    for (int d = 0; d < 2; ++d) {
+    for (int d = 0; d < kAccBufs; ++d) {
       mbar_init(&dfull[d], 1);
       mbar_init(&dempty[d], kEpiWarps);
     }
@@ -139,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmAs);
   }
   tc_fence_before();
   __syncthreads();
@@ -174,9 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + size_t(s) * kStageBytes;
           uint8_t* sb = sa + kStageA;
-          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          mbar_arrive_expect_tx(&full[s], kStageBytes + kStageAs);
           tma_load_2d(sa, &tmA, &full[s], kb * BK, mt * BM);
           tma_load_2d_hint(sb, &tmB, &full[s], kb * BK, nt * BN, pol_b);
+          tma_load_2d(as_stage + s * BM, &tmAs, &full[s], mt * BM, kb);
         }
       }
       if (!ok) {
@@ -194,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = kb_begin; kb < kb_end; ++kb, ++it, ++acc_it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          const int d = acc_it & 1;
-          const uint32_t dph = (acc_it >> 1) & 1u;
+          const int d = acc_it % kAccBufs;
+          const uint32_t dph = (acc_it / kAccBufs) & 1u;
           if (!mbar_wait(&dempty[d], dph ^ 1u, abort_flag)) {
             raise_error(err, abort_flag, kSiteMmaAccEmpty);
             ok = false;
@@ -225,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue
-    uint32_t acc_it = 0;
+    uint32_t it = 0;       // stage counter, in step with the producer and the MMA issuer
     bool ok = true;
     for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
       int mt, nt;
@@ -236,12 +246,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = m < M;
 #pragma unroll
       for (int j = 0; j < kColsPerThread; ++j) acc[j] = 0.f;
+      // Weight scales of this tile: lane j holds Bs[nt, kb0 + j] for a window
+      // of 32 K blocks, handed out by shuffle (one load per 32 blocks).
       const float* bs_row = Bs + size_t(nt) * kblocks;
-      for (int kb = kb_begin; kb < kb_end; ++kb, ++acc_it) {
-        const int d = acc_it & 1;
-        const uint32_t dph = (acc_it >> 1) & 1u;
-        const float sa = row_ok ? __ldg(As + size_t(kb) * lds + m) : 0.f;
-        const float sb = __ldg(bs_row + kb);
+      float bs_win = 0.f;
+      for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+        const int rel = kb - kb_begin;
+        if ((rel & 31) == 0) bs_win = (kb + lane < kb_end) ? __ldg(bs_row + kb + lane) : 0.f;
+        const float sb = __shfl_sync(0xffffffffu, bs_win, rel & 31);
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        const int d = it % kAccBufs;
+        const uint32_t dph = (it / kAccBufs) & 1u;
+        // Activation scales of this K block arrived with the A/B tiles.
+        const bool got_s = __all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag));
+        if (!got_s) {
+          raise_error(err, abort_flag, kSiteEpilogueFull);
+          ok = false;
+          break;
+        }
+        const float sa = as_stage[s * BM + row_in_tile];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
         // The decision must be warp-uniform: tcgen05.ld below is .sync.aligned.
         const bool got = __all_sync(0xffffffffu, mbar_wait(&dfull[d], dph, abort_flag));
         if (!got) {
@@ -349,7 +375,7 @@ cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaS
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_kernel, p.tmA, p.tmB, p.As, p.lds, p.Bs,
+  return cudaLaunchKernelEx(&cfg, w8a8_kernel, p.tmA, p.tmB, p.tmAs, p.Bs,
                             static_cast<__nv_bfloat16*>(p.C), p.ldc, p.M, p.N, p.K, split, p.err);
 }
 

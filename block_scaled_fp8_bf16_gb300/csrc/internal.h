@@ -70,8 +70,7 @@ cudaError_t launch_debug_decode(const void* codes, int64_t n, int exp_shift, voi
 struct GemmW8A8Args {
   CUtensorMap tmA;    // e4m3 [M, K], box {128 (K), 128 (M)}, 128B swizzle
   CUtensorMap tmB;    // e4m3 [N, K], box {128 (K), kW8A8TileN (N)}, 128B swizzle
-  const float* As;    // [K/128][lds]
-  int64_t lds;
+  CUtensorMap tmAs;   // fp32 [K/128][lds] read as {M, K/128}, box {128, 1}, no swizzle
   const float* Bs;    // [N/128][K/128]
   void* C;            // bf16 [M, ldc]
   int64_t ldc;

@@ -6,14 +6,15 @@
 // warp-per-group shape the ArcKernels PR proposes in its "Route-2 handover"
 // (finding 3: one warp per 128-block, shuffle max reduction, vectorised
 // loads) instead of a 1024-thread block with 32 active threads: here each
-// warp takes two adjacent 128-groups of one row, sixteen lanes per group and
-// eight bf16 per lane (one 16-byte load), reduces |x| with four xor shuffles,
-// and writes eight codes per lane (one 8-byte store).  The pass reads 2 bytes
-// and writes 1 + 4/128 bytes per element and is bound by HBM bandwidth.
+// warp takes two adjacent 128-groups of four consecutive rows, sixteen lanes
+// per group and eight bf16 per lane (one 16-byte load per row, four in
+// flight), reduces |x| with four xor shuffles, and writes eight codes per
+// lane (one 8-byte store).  The pass reads 2 bytes and writes 1 + 4/128
+// bytes per element and is bound by HBM bandwidth.
 //
-// The scale is s = amax / 448 with IEEE division, the codes are
-// e4m3(x / s) with IEEE division, round-to-nearest-even and saturation to
-// +-448 (cvt.rn.satfinite); amax == 0 gives s = 1.
+// The scale is s = amax / 448 with IEEE division; the codes are
+// e4m3(x / s) with the correctly rounded quotient, round-to-nearest-even and
+// saturation to +-448 (cvt.rn.satfinite); amax == 0 gives s = 1.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -45,42 +46,92 @@ __device__ __forceinline__ float group_scale(float amax) {
   return amax == 0.f ? 1.0f : __fdiv_rn(amax, kE4M3Max);
 }
 
-// One warp = two 128-groups (g0, g0+1) of one row.  Work items are ordered
-// row-fastest so that neighbouring warps write neighbouring scales.
+// Correctly rounded float32 quotient x / s from the correctly rounded
+// reciprocal y = RN(1/s) by one Markstein correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(x*y) is faithful, the
+// residual r = x - q0*s is exact with FMA, and RN(q0 + r*y) is RN(x/s) when
+// nothing underflows.
+//
+// The scale is first brought into [2^-60, 2^64] by exact power-of-two factors
+// applied to both operands (the quotient is unchanged); there every quotient
+// that can decide an e4m3 code (|x/s| >= 2^-11) keeps q0, r and y normal.
+// Quotients below that round to a signed zero code either way.
+struct Divisor {
+  float s;      // scaled divisor
+  float y;      // RN(1 / s)
+  float m1, m2; // factors applied to the dividend (1 when s needed no scaling)
+  bool scaled;
+};
+
+__device__ __forceinline__ Divisor make_divisor(float s) {
+  Divisor d{s, 0.f, 1.f, 1.f, false};
+  if (d.s < 0x1p-60f) {
+    d.s *= 0x1p64f;
+    d.m1 = 0x1p64f;
+    d.scaled = true;
+    if (d.s < 0x1p-60f) {
+      d.s *= 0x1p64f;
+      d.m2 = 0x1p64f;
+    }
+  } else if (d.s > 0x1p64f) {
+    d.s *= 0x1p-64f;
+    d.m1 = 0x1p-64f;
+    d.scaled = true;
+  }
+  d.y = __frcp_rn(d.s);
+  return d;
+}
+
+__device__ __forceinline__ float quotient(float x, const Divisor& d) {
+  if (d.scaled) x = __fmul_rn(__fmul_rn(x, d.m1), d.m2);
+  const float q0 = __fmul_rn(x, d.y);
+  const float r = __fmaf_rn(-q0, d.s, x);
+  return __fmaf_rn(r, d.y, q0);
+}
+
+// Grid: x covers rows (each warp takes kQuantRows consecutive rows per
+// step), y covers pairs of 128-groups (lanes 0-15: group 2y, 16-31: 2y+1).
+constexpr int kQuantRows = 4;
+
 __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
                                                         int64_t ldx, uint8_t* __restrict__ a, int64_t lda,
                                                         float* __restrict__ scales, int64_t lds) {
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;
   const int hl = lane & 15;
-  const int64_t groups = K / 128;
-  const int64_t pairs = (groups + 1) / 2;
-  const int64_t items = M * pairs;
-  const int64_t warps_total = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < items; w += warps_total) {
-    const int64_t m = w % M;
-    const int64_t g = (w / M) * 2 + half;
-    const bool active = g < groups;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    const int64_t col = g * 128 + hl * 8;
-    if (active) v = ld_nc_v4(x + m * ldx + col);
-    float f[8];
-    bf16x8_to_f32(v, f);
-    float amax = 0.f;
+  const int64_t g = int64_t(blockIdx.y) * 2 + (lane >> 4);
+  const bool active = g < K / 128;
+  const int64_t col = g * 128 + hl * 8;
+  const int64_t step = int64_t(gridDim.x) * (blockDim.x >> 5) * kQuantRows;
+  for (int64_t m0 = (int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kQuantRows; m0 < M;
+       m0 += step) {
+    uint4 v[kQuantRows];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    for (int r = 0; r < kQuantRows; ++r) {
+      v[r] = make_uint4(0, 0, 0, 0);
+      if (active && m0 + r < M) v[r] = ld_nc_v4(x + (m0 + r) * ldx + col);
+    }
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = group_scale(amax);
-    float q[8];
+    for (int r = 0; r < kQuantRows; ++r) {
+      float f[8];
+      bf16x8_to_f32(v[r], f);
+      float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(f[i], s);
-    if (active) {
-      uint2 out;
-      out.x = e4m3x4(q[0], q[1], q[2], q[3]);
-      out.y = e4m3x4(q[4], q[5], q[6], q[7]);
-      *reinterpret_cast<uint2*>(a + m * lda + col) = out;
-      if (hl == 0) scales[g * lds + m] = s;
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float s = group_scale(amax);
+      const Divisor dv = make_divisor(s);
+      float q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = quotient(f[i], dv);
+      if (active && m0 + r < M) {
+        uint2 out;
+        out.x = e4m3x4(q[0], q[1], q[2], q[3]);
+        out.y = e4m3x4(q[4], q[5], q[6], q[7]);
+        *reinterpret_cast<uint2*>(a + (m0 + r) * lda + col) = out;
+        if (hl == 0) scales[g * lds + m0 + r] = s;
+      }
     }
   }
 }
@@ -114,6 +165,7 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __nv_bfloat16* 
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
   const float s = group_scale(amax);
+  const Divisor dv = make_divisor(s);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int i = tid + 256 * j;
@@ -121,8 +173,8 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __nv_bfloat16* 
     float f[8];
     bf16x8_to_f32(v[j], f);
     uint2 out;
-    out.x = e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
-    out.y = e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+    out.x = e4m3x4(quotient(f[0], dv), quotient(f[1], dv), quotient(f[2], dv), quotient(f[3], dv));
+    out.y = e4m3x4(quotient(f[4], dv), quotient(f[5], dv), quotient(f[6], dv), quotient(f[7], dv));
     *reinterpret_cast<uint2*>(b + (nb * 128 + r) * ldb + kb * 128 + c * 8) = out;
   }
   if (tid == 0) scales[nb * kb_count + kb] = s;
@@ -189,9 +241,14 @@ int grid_for(int64_t items, int per_block, int num_sms, int waves) {
 }  // namespace
 
 cudaError_t launch_quant_act(const QuantActArgs& p, const DeviceInfo& dev, cudaStream_t s) {
-  const int64_t items = p.M * ((p.K / 128 + 1) / 2);   // warps of work
-  const int grid = grid_for(items, 8, dev.num_sms, 16);
-  quant_act_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(p.x), p.M, p.K, p.ldx,
+  const int64_t pairs = (p.K / 128 + 1) / 2;
+  if (pairs > 65535) return cudaErrorInvalidValue;
+  const int64_t row_steps = (p.M + kQuantRows - 1) / kQuantRows;     // warps needed along M
+  int64_t gx = (row_steps + 7) / 8;
+  const int64_t cap = (int64_t(dev.num_sms) * 16 + pairs - 1) / pairs;  // about 16 CTAs per SM in total
+  if (gx > cap) gx = cap;
+  if (gx < 1) gx = 1;
+  quant_act_kernel<<<dim3(unsigned(gx), unsigned(pairs)), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(p.x), p.M, p.K, p.ldx,
                                         static_cast<uint8_t*>(p.a), p.lda, p.scales, p.lds);
   return cudaGetLastError();
 }

@@ -110,3 +110,27 @@ def test_validate_weights_counts(lib):
     e[3, 3] = 127 + 7
     b2 = synth.finite_e4m3_codes(2, (256, 512))
     assert fp8blk.validate_weights(to_dev(b2), to_dev(e), fp8blk.SCALE_UE8M0_32x32) == (0, 2)
+
+
+def test_quant_act_many_scales_across_the_exponent_range(lib):
+    """400 group maxima spread over the whole bf16 exponent range (tiny,
+    denormal and huge scales included), 1023 random companions each."""
+    rng = np.random.default_rng(21)
+    allb = np.arange(65536, dtype=np.uint16)
+    vals = O.bf16_bits_to_f64(allb)
+    fin_pos = allb[np.isfinite(vals) & (vals > 0)]
+    amaxes = np.concatenate([rng.choice(fin_pos, 392, replace=False),
+                             np.array([0x0001, 0x0002, 0x0080, 0x0F80, 0x1000, 0x6F80, 0x7F7F, 0x43E0],
+                                      dtype=np.uint16)])
+    rows = []
+    for ab in amaxes:
+        a = O.bf16_bits_to_f64(np.array([ab], dtype=np.uint16))[0]
+        pool = allb[np.isfinite(vals) & (np.abs(vals) <= a)]
+        g = rng.choice(pool, 1024)
+        g[rng.integers(0, 1024)] = ab | (rng.integers(0, 2) << 15)
+        rows.append(g.reshape(8, 128))
+    x = np.concatenate(rows, axis=0).reshape(-1, 256)        # two groups per row
+    a, s, _ = gpu_quant_act(x)
+    qa, qs = O.quant_act_1x128(x)
+    assert np.array_equal(s[:, : x.shape[0]].view(np.uint32), qs.view(np.uint32))
+    assert np.array_equal(a, qa)
