@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libfp8blk.so")
-SOURCES = ["api.cu", "quant.cu", "gemm_w8a8.cu", "gemm_w8a16.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm_w8a8.cu", "gemm_w8a8_pair.cu", "gemm_w8a16.cu"]
 HEADERS = ["ptx.cuh", "decode.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
@@ -58,8 +58,16 @@ def _compile(nvcc, src):
     return src, obj, r.returncode, r.stdout + r.stderr, cmd
 
 
+# Kernels that rebalance registers between warpgroups with setmaxnreg: the
+# split is computed for exactly this many registers per thread at launch, so
+# any other count must stop the build (a split larger than the launch
+# allocation would wait forever).
+SETMAXNREG_KERNELS = {"w8a8_pair_kernel": 168}
+
+
 def check_resources(log: str) -> list[str]:
-    """Kernels whose ptxas report shows spill stores/loads or a stack frame."""
+    """Kernels whose ptxas report shows spill stores/loads or a stack frame,
+    or a register count other than the one their register split assumes."""
     bad = []
     current = None
     for line in log.splitlines():
@@ -69,6 +77,11 @@ def check_resources(log: str) -> list[str]:
         m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads", line)
         if m and current and any(int(v) for v in m.groups()):
             bad.append(f"{current}: {line.strip()}")
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current:
+            for name, regs in SETMAXNREG_KERNELS.items():
+                if name in current and int(m.group(1)) != regs:
+                    bad.append(f"{current}: {m.group(1)} registers, register split assumes {regs}")
     return bad
 
 

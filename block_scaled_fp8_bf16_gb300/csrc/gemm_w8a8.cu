@@ -339,6 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  // Enough 256x256 tiles to keep most CTA pairs busy: the pair kernel.
+  if (p.M > kW8A8TileM && 2 * w8a8_pair_tiles(p.M, p.N) >= dev.num_sms / 2) return launch_gemm_w8a8_pair(p, dev, stream);
   static bool attr_done[64] = {};
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);

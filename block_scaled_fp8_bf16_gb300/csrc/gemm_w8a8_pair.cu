@@ -1,0 +1,378 @@
+// W8A8 block-scaled FP8 GEMM on CTA pairs (tcgen05 .cta_group::2), sm_103a.
+//
+// Same arithmetic as the single-CTA kernel in gemm_w8a8.cu: one FP32 partial
+// per 128-wide K block from e4m3 operands only, promoted once with
+// As[kb, m] * Bs[n/128, kb] ("Blockwise FP8 on Ada GPUs, part 2", "The fix").
+// Here two CTAs of a cluster form one 256 x 256 output tile: each CTA loads
+// its 128 rows of A and its 128 rows of B (N) per K block, and one thread of
+// the even CTA issues M = 256, N = 256, K = 32 MMAs that read both CTAs'
+// shared memory and write each CTA's 128 rows of the partial into its own
+// TMEM.  Per SM this halves the operand bytes fetched from L2 and read from
+// shared memory per FLOP compared with a 128 x 128 single-CTA tile, which is
+// what bounds the single-CTA kernel on large problems.
+//
+// Roles per CTA (three warpgroups; registers are rebalanced with setmaxnreg
+// from 168 per thread at launch to 40 for warpgroup 0 and 232 for the two
+// epilogue warpgroups: 40*128 + 232*256 = 168*384, which the build checks):
+//   warp 0       TMA producer for this CTA's A rows, B rows and scales.
+//   warp 1       TMEM allocation (with the peer, 512 columns = two 256-column
+//                partials); in the even CTA one thread issues the MMAs and
+//                commits to both CTAs' barriers; in the odd CTA one thread
+//                forwards "stage landed" to the even CTA's barrier.
+//   warps 4..11  promotion + epilogue, 8 warps: TMEM lane quarter = warp % 4,
+//                128 of the 256 columns each; acc = fma(partial, As*Bs, acc);
+//                bf16 store at the end of the tile.
+// Tiles of the pair run persistently in grouped raster order ("Blockwise FP8
+// on Ada GPUs, part 2", "One tile doesn't fit all M": launch-order swizzle).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8blk {
+namespace {
+
+constexpr int TM = 128;              // A rows per CTA (256 per pair)
+constexpr int PN = 256;              // C columns per pair tile (MMA N)
+constexpr int HN = PN / 2;           // B rows per CTA
+constexpr int BK = 128;              // one scale block of K
+constexpr int kStages = 6;
+constexpr int kStageA = TM * BK;
+constexpr int kStageB = HN * BK;
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kStageAs = TM * 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 128 + kEpiWarps * 32;   // 384: three warpgroups
+constexpr int kCols = PN / (kEpiWarps / 4);      // 128 columns per epilogue thread
+constexpr int kChunk = 32;                       // columns per tcgen05.ld
+constexpr int kRegsLaunch = 168;                 // registers per thread at launch (checked at build time)
+constexpr int kRegsWg0 = 40;
+constexpr int kRegsEpi = 232;
+static_assert(kRegsWg0 * 128 + kRegsEpi * 256 <= kRegsLaunch * kThreads, "register split");
+constexpr int kAccBufs = 2;
+constexpr uint32_t kTmemCols = kAccBufs * PN;
+constexpr uint32_t kIdesc = make_idesc(0 /* e4m3 */, 2 * TM, PN);
+constexpr int kGroupM = 8;
+constexpr int kBarrierBytes = 512;
+constexpr size_t kSmemBytes = size_t(kStages) * (kStageBytes + kStageAs) + kBarrierBytes + 1024;
+
+static_assert(kTmemCols == 512, "two 256-column partials fill TMEM");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "swizzle atoms");
+
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mt, int& nt) {
+  const int per_group = kGroupM * n_tiles;
+  const int g = t / per_group;
+  const int first = g * kGroupM;
+  const int gsz = min(m_tiles - first, kGroupM);
+  const int r = t - g * per_group;
+  mt = first + r % gsz;
+  nt = r / gsz;
+}
+
+__device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, int site) {
+  *abort_flag = 1;
+  atomicCAS(err, 0, kDevErrW8A8 | 0x80 | site);
+}
+
+// try_wait with cluster-scope acquire, for phases completed by the peer CTA.
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_test_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_cluster(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const float2* acc) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < kCols / 8; ++i) {
+    uint4 v;
+    v.x = pack_bf16x2(acc[4 * i + 0].x, acc[4 * i + 0].y);
+    v.y = pack_bf16x2(acc[4 * i + 1].x, acc[4 * i + 1].y);
+    v.z = pack_bf16x2(acc[4 * i + 2].x, acc[4 * i + 2].y);
+    v.w = pack_bf16x2(acc[4 * i + 3].x, acc[4 * i + 3].y);
+    d[i] = v;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    w8a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmAs, const float* __restrict__ Bs,
+                     __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N, int K, int* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  float* as_stage = reinterpret_cast<float*>(smem + size_t(kStages) * kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * (kStageBytes + kStageAs));
+  uint64_t* peer_full = full + kStages;
+  uint64_t* empty = peer_full + kStages;
+  uint64_t* dfull = empty + kStages;
+  uint64_t* dempty = dfull + kAccBufs;
+  uint64_t* drain = dempty + kAccBufs;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  const int m_tiles = (M + 2 * TM - 1) / (2 * TM);
+  const int n_tiles = (N + PN - 1) / PN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int kblocks = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&peer_full[s], 1);
+      mbar_init(&empty[s], 1 + kEpiWarps);   // MMA done with A/B, epilogue done with the scales
+    }
+    for (int d = 0; d < kAccBufs; ++d) {
+      mbar_init(&dfull[d], 1);
+      mbar_init(&dempty[d], 2 * kEpiWarps);   // both CTAs' epilogues (used in the even CTA)
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmAs);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // the peer's barriers exist before any commit or arrive reaches them
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
+    if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+        int mt, nt;
+        tile_coords(t, m_tiles, n_tiles, mt, nt);
+        const int m0 = mt * 2 * TM + rank * TM;
+        const int n0 = nt * PN + rank * HN;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteProducerEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + size_t(s) * kStageBytes;
+          mbar_arrive_expect_tx(&full[s], kStageBytes + kStageAs);
+          tma_load_2d(sa, &tmA, &full[s], kb * BK, m0);
+          tma_load_2d(sa + kStageA, &tmB, &full[s], kb * BK, n0);
+          tma_load_2d(as_stage + s * TM, &tmAs, &full[s], m0, kb);
+        }
+      }
+      if (!ok) {
+        const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1u, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------- MMA issuer (even CTA)
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+        for (int kb = 0; kb < kblocks; ++kb, ++it, ++acc_it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          const int d = acc_it % kAccBufs;
+          const uint32_t dph = (acc_it / kAccBufs) & 1u;
+          if (!mbar_wait_cluster(&dempty[d], dph ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaAccEmpty);
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&full[s], ph, abort_flag) || !mbar_wait_cluster(&peer_full[s], ph, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaFull);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + size_t(s) * kStageBytes);
+          const uint32_t b0 = a0 + kStageA;
+          const uint32_t d_tmem = tmem + uint32_t(d * PN);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            mma_f8_ss_pair(d_tmem, desc_sw128_kmajor(a0 + 32u * k), desc_sw128_kmajor(b0 + 32u * k), kIdesc,
+                           k > 0 ? 1u : 0u);
+          }
+          mma_commit_pair_mc(&empty[s], 0x3);
+          mma_commit_pair_mc(&dfull[d], 0x3);
+        }
+      }
+      mma_commit_pair_mc(drain, 0x1);
+      mbar_wait(drain, 0, nullptr);
+    } else if (lane == 0) {
+      // ---------------------------------------------------------- relay (odd CTA)
+      const uint32_t peer_full0 = map_shared_rank(smem_u32(peer_full), 0);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaFull);
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(peer_full0 + uint32_t(s) * 8u);
+        }
+      }
+    }
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+    // ------------------------------------------------------------ promotion + epilogue
+    const int e = warp - 4;
+    const int quarter = warp & 3;
+    const int col0 = (e >> 2) * kCols;
+    const int row = quarter * 32 + lane;
+    const uint32_t dempty0 = map_shared_rank(smem_u32(dempty), 0);
+    float2 acc[kCols / 2];
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+      int mt, nt;
+      tile_coords(t, m_tiles, n_tiles, mt, nt);
+      const int m = mt * 2 * TM + rank * TM + row;
+      const int n = nt * PN + col0;
+      const bool row_ok = m < M;
+      const bool col_ok = n < N;
+#pragma unroll
+      for (int j = 0; j < kCols / 2; ++j) acc[j] = make_float2(0.f, 0.f);
+      const float* bs_row = Bs + size_t(col_ok ? n / 128 : 0) * kblocks;
+      float bs_win = 0.f;
+      for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        if ((kb & 31) == 0) bs_win = (col_ok && kb + lane < kblocks) ? __ldg(bs_row + kb + lane) : 0.f;
+        const float sb = __shfl_sync(0xffffffffu, bs_win, kb & 31);
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        const int d = it % kAccBufs;
+        const uint32_t dph = (it / kAccBufs) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag))) {
+          raise_error(err, abort_flag, kSiteEpilogueFull);
+          ok = false;
+          break;
+        }
+        const float sa = as_stage[s * TM + row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (!__all_sync(0xffffffffu, mbar_wait(&dfull[d], dph, abort_flag))) {
+          raise_error(err, abort_flag, kSiteEpilogueFull);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float sc = sa * sb;
+        const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(d * PN + col0);
+        // 32 columns per load; the buffer is handed back as soon as the last
+        // columns are in registers.
+#pragma unroll
+        for (int c = 0; c < kCols / kChunk; ++c) {
+          uint32_t p[kChunk];
+          tmem_ld_x32(taddr + uint32_t(c * kChunk), p);
+          tmem_ld_wait();
+          if (c + 1 == kCols / kChunk) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(dempty0 + uint32_t(d) * 8u);
+          }
+#pragma unroll
+          for (int j = 0; j < kChunk; j += 2) {
+            const int i = (c * kChunk + j) / 2;
+            acc[i].x = fmaf(__uint_as_float(p[j]), sc, acc[i].x);
+            acc[i].y = fmaf(__uint_as_float(p[j + 1]), sc, acc[i].y);
+          }
+        }
+      }
+      if (ok && row_ok && col_ok) store_row(C + size_t(m) * ldc + n, acc);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // neither CTA leaves while the other may still reach its shared memory
+  // Re-read the TMEM address here instead of keeping it live across the role
+  // branches, where the register budget is the smaller warpgroup's.
+  if ((threadIdx.x >> 5) == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(*reinterpret_cast<volatile uint32_t*>(tmem_holder), kTmemCols);
+  }
+}
+
+}  // namespace
+
+int w8a8_pair_tiles(int M, int N) { return ((M + 2 * TM - 1) / (2 * TM)) * ((N + PN - 1) / PN); }
+
+cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  static bool attr_done[64] = {};
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if (device < 64 && !attr_done[device]) {
+    // The setmaxnreg split assumes the launch register count; refuse to run
+    // any build where it differs.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, w8a8_pair_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
+    e = cudaFuncSetAttribute(w8a8_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done[device] = true;
+  }
+  const int tiles = w8a8_pair_tiles(p.M, p.N);
+  const int max_pairs = dev.num_sms / 2;
+  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel, p.tmA, p.tmB, p.tmAs, p.Bs, static_cast<__nv_bfloat16*>(p.C),
+                            p.ldc, p.M, p.N, p.K, p.err);
+}
+
+}  // namespace fp8blk

@@ -81,6 +81,9 @@ constexpr int kW8A8TileM = 128;
 constexpr int kW8A8TileN = 128;
 constexpr int kMaxSplitK = 8;
 cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t s);
+// CTA-pair kernel (256 x 256 tiles); chosen by launch_gemm_w8a8 for large problems.
+int w8a8_pair_tiles(int M, int N);
+cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t s);
 
 // ------------------------------------------------------------------ W8A16
 struct GemmW8A16Args {

@@ -87,7 +87,9 @@ __device__ __forceinline__ float quotient(float x, const Divisor& d) {
   if (d.scaled) x = __fmul_rn(__fmul_rn(x, d.m1), d.m2);
   const float q0 = __fmul_rn(x, d.y);
   const float r = __fmaf_rn(-q0, d.s, x);
-  return __fmaf_rn(r, d.y, q0);
+  // s > 0, so the quotient has the dividend's sign; this also keeps -0 / s = -0,
+  // which the correction step would turn into +0.
+  return copysignf(__fmaf_rn(r, d.y, q0), x);
 }
 
 // Grid: x covers rows (each warp takes kQuantRows consecutive rows per
