@@ -14,11 +14,13 @@
 // Roles per CTA (three warpgroups; registers are rebalanced with setmaxnreg
 // from 168 per thread at launch to 40 for warpgroup 0 and 232 for the two
 // epilogue warpgroups: 40*128 + 232*256 = 168*384, which the build checks):
-//   warp 0       TMA producer for this CTA's A rows, B rows and scales.
+//   warps 0, 2   TMA producers for this CTA's A rows + scales (warp 0) and B
+//                rows (warp 2).
 //   warp 1       TMEM allocation (with the peer, 512 columns = two 256-column
 //                partials); in the even CTA one thread issues the MMAs and
-//                commits to both CTAs' barriers; in the odd CTA one thread
-//                forwards "stage landed" to the even CTA's barrier.
+//                commits to both CTAs' barriers.  Both CTAs' operand copies
+//                complete on the even CTA's stage barrier (.cta_group::2
+//                TMA), so the MMA issuer waits on one barrier per stage.
 //   warps 4..11  promotion + epilogue, 8 warps: TMEM lane quarter = warp % 4,
 //                128 of the 256 columns each; acc = fma(partial, As*Bs, acc);
 //                bf16 store at the end of the tile.
@@ -41,6 +43,7 @@ constexpr int kStageA = TM * BK;
 constexpr int kStageB = HN * BK;
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kStageAs = TM * 4;
+constexpr int kAsStages = 16;        // scale ring, deeper than the operand ring so it never gates it
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + kEpiWarps * 32;   // 384: three warpgroups
 constexpr int kCols = PN / (kEpiWarps / 4);      // 128 columns per epilogue thread
@@ -53,8 +56,8 @@ constexpr int kAccBufs = 2;
 constexpr uint32_t kTmemCols = kAccBufs * PN;
 constexpr uint32_t kIdesc = make_idesc(0 /* e4m3 */, 2 * TM, PN);
 constexpr int kGroupM = 8;
-constexpr int kBarrierBytes = 512;
-constexpr size_t kSmemBytes = size_t(kStages) * (kStageBytes + kStageAs) + kBarrierBytes + 1024;
+constexpr int kBarrierBytes = 1024;
+constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + size_t(kAsStages) * kStageAs + kBarrierBytes + 1024;
 
 static_assert(kTmemCols == 512, "two 256-column partials fill TMEM");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -120,11 +123,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  float* as_stage = reinterpret_cast<float*>(smem + size_t(kStages) * kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * (kStageBytes + kStageAs));
-  uint64_t* peer_full = full + kStages;
-  uint64_t* empty = peer_full + kStages;
-  uint64_t* dfull = empty + kStages;
+  float* as_stage = reinterpret_cast<float*>(smem + size_t(kStages) * kStageBytes);   // [kAsStages][TM]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes + size_t(kAsStages) * kStageAs);
+  uint64_t* empty = full + kStages;
+  uint64_t* as_full = empty + kStages;
+  uint64_t* as_empty = as_full + kAsStages;
+  uint64_t* dfull = as_empty + kAsStages;
   uint64_t* dempty = dfull + kAccBufs;
   uint64_t* drain = dempty + kAccBufs;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -142,9 +146,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&peer_full[s], 1);
-      mbar_init(&empty[s], 1 + kEpiWarps);   // MMA done with A/B, epilogue done with the scales
+      mbar_init(&full[s], 2);                // A and B producers of the even CTA; both CTAs' bytes
+      mbar_init(&empty[s], 1);               // MMA done with A/B
+    }
+    for (int j = 0; j < kAsStages; ++j) {
+      mbar_init(&as_full[j], 1);
+      mbar_init(&as_empty[j], kEpiWarps);    // this CTA's epilogue done with the scales
     }
     for (int d = 0; d < kAccBufs; ++d) {
       mbar_init(&dfull[d], 1);
@@ -170,8 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
-    if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ producers
+    // Two issuing threads (A + scales from warp 0, B from warp 2): one thread
+    // alone cannot issue strided 128-byte-row tiles at the rate the MMAs use.
+    const bool a_side = warp == 0;
+    const uint32_t full0_base = map_shared_rank(smem_u32(full), 0);
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -183,21 +194,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
+          const int j = it % kAsStages;
+          const uint32_t jph = (it / kAsStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag) ||
+              (a_side && !mbar_wait(&as_empty[j], jph ^ 1u, abort_flag))) {
             raise_error(err, abort_flag, kSiteProducerEmpty);
             ok = false;
             break;
           }
           uint8_t* sa = smem + size_t(s) * kStageBytes;
-          mbar_arrive_expect_tx(&full[s], kStageBytes + kStageAs);
-          tma_load_2d(sa, &tmA, &full[s], kb * BK, m0);
-          tma_load_2d(sa + kStageA, &tmB, &full[s], kb * BK, n0);
-          tma_load_2d(as_stage + s * TM, &tmAs, &full[s], m0, kb);
+          // Operand tiles of both CTAs complete on the even CTA's full[s]:
+          // its producers announce the pair's bytes, the odd CTA's loads
+          // only deliver them.
+          const uint32_t full0 = full0_base + uint32_t(s) * 8u;
+          if (a_side) {
+            mbar_arrive_expect_tx(&as_full[j], kStageAs);
+            tma_load_2d(as_stage + j * TM, &tmAs, &as_full[j], m0, kb);
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kStageA);
+            tma_load_2d_pair(sa, &tmA, full0, kb * BK, m0);
+          } else {
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kStageB);
+            tma_load_2d_pair(sa + kStageA, &tmB, full0, kb * BK, n0);
+          }
         }
       }
       if (!ok) {
+        // Let issued copies land before the CTA can exit (the odd CTA's
+        // operand copies complete on the even CTA's barrier; they finish
+        // within microseconds, long before any bounded wait gives up).
         const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0u;
-        for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1u, nullptr);
+        if (rank == 0)
+          for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1u, nullptr);
+        const uint32_t first_as = it > uint32_t(kAsStages) ? it - kAsStages : 0u;
+        if (a_side)
+          for (uint32_t j = first_as; j < it; ++j) mbar_wait(&as_full[j % kAsStages], (j / kAsStages) & 1u, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -216,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (!mbar_wait(&full[s], ph, abort_flag) || !mbar_wait_cluster(&peer_full[s], ph, abort_flag)) {
+          if (!mbar_wait_cluster(&full[s], ph, abort_flag)) {
             raise_error(err, abort_flag, kSiteMmaFull);
             ok = false;
             break;
@@ -236,23 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit_pair_mc(drain, 0x1);
       mbar_wait(drain, 0, nullptr);
-    } else if (lane == 0) {
-      // ---------------------------------------------------------- relay (odd CTA)
-      const uint32_t peer_full0 = map_shared_rank(smem_u32(peer_full), 0);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
-          if (!mbar_wait(&full[s], ph, abort_flag)) {
-            raise_error(err, abort_flag, kSiteMmaFull);
-            ok = false;
-            break;
-          }
-          mbar_arrive_cluster(peer_full0 + uint32_t(s) * 8u);
-        }
-      }
     }
     }
   } else {
@@ -280,18 +293,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         if ((kb & 31) == 0) bs_win = (col_ok && kb + lane < kblocks) ? __ldg(bs_row + kb + lane) : 0.f;
         const float sb = __shfl_sync(0xffffffffu, bs_win, kb & 31);
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1u;
+        const int j = it % kAsStages;
+        const uint32_t jph = (it / kAsStages) & 1u;
         const int d = it % kAccBufs;
         const uint32_t dph = (it / kAccBufs) & 1u;
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&as_full[j], jph, abort_flag))) {
           raise_error(err, abort_flag, kSiteEpilogueFull);
           ok = false;
           break;
         }
-        const float sa = as_stage[s * TM + row];
+        const float sa = as_stage[j * TM + row];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) mbar_arrive(&as_empty[j]);
         if (!__all_sync(0xffffffffu, mbar_wait(&dfull[d], dph, abort_flag))) {
           raise_error(err, abort_flag, kSiteEpilogueFull);
           ok = false;
@@ -310,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c + 1 == kCols / kChunk) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(dempty0 + uint32_t(d) * 8u);
+            if (lane == 0) mbar_arrive_cluster_relaxed(dempty0 + uint32_t(d) * 8u);
           }
 #pragma unroll
           for (int j = 0; j < kChunk; j += 2) {
