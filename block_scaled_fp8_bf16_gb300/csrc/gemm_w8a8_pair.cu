@@ -313,20 +313,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float sc = sa * sb;
         const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(d * PN + col0);
-        // 32 columns per load; the buffer is handed back as soon as the last
-        // columns are in registers.
+        // Two 32-column loads per wait; the buffer is handed back as soon as
+        // the last columns are in registers.
 #pragma unroll
-        for (int c = 0; c < kCols / kChunk; ++c) {
-          uint32_t p[kChunk];
+        for (int c = 0; c < kCols / kChunk; c += 2) {
+          uint32_t p[2 * kChunk];
           tmem_ld_x32(taddr + uint32_t(c * kChunk), p);
+          tmem_ld_x32(taddr + uint32_t((c + 1) * kChunk), p + kChunk);
           tmem_ld_wait();
-          if (c + 1 == kCols / kChunk) {
+          if (c + 2 == kCols / kChunk) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(dempty0 + uint32_t(d) * 8u);
           }
 #pragma unroll
-          for (int j = 0; j < kChunk; j += 2) {
+          for (int j = 0; j < 2 * kChunk; j += 2) {
             const int i = (c * kChunk + j) / 2;
             acc[i].x = fmaf(__uint_as_float(p[j]), sc, acc[i].x);
             acc[i].y = fmaf(__uint_as_float(p[j + 1]), sc, acc[i].y);
