@@ -46,8 +46,8 @@ namespace {
 constexpr int BN = kW8A16TileN;   // weight rows per tile (MMA M)
 constexpr int BK = 128;           // K per block (one fp32 scale block)
 constexpr int kStageW = BN * BK;  // 16 KB of e4m3
-constexpr int kDecWarps = 4;
 constexpr int kACols = BK / 2;    // TMEM columns of one decoded A block (2 bf16 per column)
+constexpr int kABufs = 4;         // decoded A blocks in flight in TMEM
 constexpr int kGroupN = 8;
 constexpr int kBarrierBytes = 512;
 
@@ -57,13 +57,20 @@ struct Cfg {
   // tile, where two warps share a lane quarter and split the columns.
   static constexpr int kEpiWarps = TM >= 128 ? 8 : 4;
   static constexpr int kEpiCols = TM / (kEpiWarps / 4);
+  // Decode warps: two per TMEM lane quarter (each decodes half of the K
+  // block) unless the epilogue already needs eight warps.
+  static constexpr int kDecWarps = TM >= 64 ? 4 : 8;
+  static constexpr int kDecChunks = 8 / (kDecWarps / 4);   // 16-byte chunks of a row per decode warp
   static constexpr int kThreads = 64 + (kDecWarps + kEpiWarps) * 32;
   static constexpr int kStageX = TM * BK * 2;                  // bf16 activation tile
   static constexpr int kStageBytes = kStageW + kStageX;
   // One CTA per SM (registers are allocated per 4-warp group, so a second
   // 10..14-warp CTA would not fit); the ring is as deep as shared memory allows.
   static constexpr int kStages = TM == 16 ? 8 : (TM == 32 ? 7 : (TM == 64 ? 5 : 4));
-  static constexpr uint32_t kTmemUsed = 2 * kACols + 2 * TM;
+  // FP32 partial buffers: as many as fit next to the A blocks (the promotion
+  // round trip per K block is long compared with a narrow tile's MMA time).
+  static constexpr int kDBufs = TM <= 32 ? 8 : (TM == 64 ? 4 : 2);
+  static constexpr uint32_t kTmemUsed = kABufs * kACols + kDBufs * TM;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
   static constexpr uint32_t kIdesc = make_idesc(1 /* bf16 */, BN, TM);
   static constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + kBarrierBytes + 1024;
@@ -112,10 +119,10 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(Q::kStages) * Q::kStageBytes);
   uint64_t* empty = full + Q::kStages;
   uint64_t* afull = empty + Q::kStages;
-  uint64_t* aempty = afull + 2;
-  uint64_t* dfull = aempty + 2;
-  uint64_t* dempty = dfull + 2;
-  uint64_t* drain = dempty + 2;
+  uint64_t* aempty = afull + kABufs;
+  uint64_t* dfull = aempty + kABufs;
+  uint64_t* dempty = dfull + Q::kDBufs;
+  uint64_t* drain = dempty + Q::kDBufs;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -135,11 +142,13 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
   if (threadIdx.x == 0) {
     for (int s = 0; s < Q::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kDecWarps + 1);   // decoders done with W, MMA done with X
+      mbar_init(&empty[s], Q::kDecWarps + 1);   // decoders done with W, MMA done with X
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&afull[i], kDecWarps);
+    for (int i = 0; i < kABufs; ++i) {
+      mbar_init(&afull[i], Q::kDecWarps);
       mbar_init(&aempty[i], 1);
+    }
+    for (int i = 0; i < Q::kDBufs; ++i) {
       mbar_init(&dfull[i], 1);
       mbar_init(&dempty[i], Q::kEpiWarps);
     }
@@ -160,13 +169,13 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const uint32_t tmem_a = tmem;                 // 2 x 64 columns of decoded weights
-  const uint32_t tmem_d = tmem + 2 * kACols;    // 2 x TM columns of FP32 accumulators
+  const uint32_t tmem_d = tmem + kABufs * kACols;   // kDBufs x TM columns of FP32 accumulators
 
   constexpr int EC = Q::kEpiCols;
   float acc[EC];
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;          // weight row within the tile (TMEM lane)
-  const int col0 = warp >= 2 + kDecWarps + 4 ? EC : 0;   // second epilogue warp of a lane quarter
+  const int col0 = warp >= 2 + Q::kDecWarps + 4 ? EC : 0;   // second epilogue warp of a lane quarter
   int last_nt = 0, last_mt = 0;
 
   if (warp == 0) {
@@ -201,29 +210,23 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // A single thread issues every MMA, so its loop is kept short: ring
+    // positions advance by counters, the stage descriptor is built once per
+    // K block, and the stage's own barrier is not re-tested: "A block
+    // decoded" implies the stage landed, because every decode warp waits for
+    // the stage before it decodes.
     if (lane == 0) {
-      uint32_t it = 0, acc_it = 0;
+      uint32_t s = 0, ph = 0, a = 0, aph = 0, d = 0, dph = 0;
       bool ok = true;
       for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
-        for (int kb = kb_begin; kb < kb_end && ok; ++kb, ++it) {
-          const int s = it % Q::kStages;
-          const uint32_t ph = (it / Q::kStages) & 1u;
-          const int a = it & 1;
-          const uint32_t aph = (it >> 1) & 1u;
+        for (int kb = kb_begin; kb < kb_end && ok; ++kb) {
           const bool first_kb = kb == kb_begin;
           const bool last_kb = kb + 1 == kb_end;
           // fp32 format: one accumulator buffer per K block; UE8M0: per tile.
           const bool new_acc = !ue8m0 || first_kb;
           const bool done_acc = !ue8m0 || last_kb;
-          const int d = acc_it & 1;
-          const uint32_t dph = (acc_it >> 1) & 1u;
           if (new_acc && !mbar_wait(&dempty[d], dph ^ 1u, abort_flag)) {
             raise_error(err, abort_flag, kSiteMmaAccEmpty);
-            ok = false;
-            break;
-          }
-          if (!mbar_wait(&full[s], ph, abort_flag)) {
-            raise_error(err, abort_flag, kSiteMmaFull);
             ok = false;
             break;
           }
@@ -233,27 +236,34 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
             break;
           }
           tc_fence_after();
-          const uint32_t x0 = smem_u32(smem + size_t(s) * Q::kStageBytes + kStageW);
-          const uint32_t d_tmem = tmem_d + uint32_t(d * TM);
+          const uint64_t xdesc = desc_sw128_kmajor(smem_u32(smem + size_t(s) * Q::kStageBytes + kStageW));
+          const uint32_t d_tmem = tmem_d + d * uint32_t(TM);
+          const uint32_t a_tmem = tmem_a + a * uint32_t(kACols);
 #pragma unroll
           for (int j = 0; j < BK / 16; ++j) {
-            const uint32_t xa = x0 + uint32_t((j >> 2) * TM * 128 + (j & 3) * 32);
-            mma_bf16_ts(d_tmem, tmem_a + uint32_t(a * kACols + j * 8), desc_sw128_kmajor(xa), Q::kIdesc,
-                        (j > 0 || !new_acc) ? 1u : 0u);
+            // advance the start-address field (16-byte units) to k-step j
+            const uint64_t xd = xdesc + uint64_t(((j >> 2) * TM * 128 + (j & 3) * 32) >> 4);
+            mma_bf16_ts(d_tmem, a_tmem + uint32_t(j * 8), xd, Q::kIdesc, (j > 0 || !new_acc) ? 1u : 0u);
           }
           mma_commit(&empty[s]);
           mma_commit(&aempty[a]);
           if (done_acc) {
             mma_commit(&dfull[d]);
-            ++acc_it;
+            if (++d == uint32_t(Q::kDBufs)) { d = 0; dph ^= 1u; }
           }
+          if (++s == uint32_t(Q::kStages)) { s = 0; ph ^= 1u; }
+          if (++a == uint32_t(kABufs)) { a = 0; aph ^= 1u; }
         }
       }
+      (void)ph;
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else if (warp < 2 + kDecWarps) {
+  } else if (warp < 2 + Q::kDecWarps) {
     // ------------------------------------------------------------ decode
+    // First 16-byte chunk of the row this warp decodes (second warp of a
+    // lane quarter takes the upper half of the K block).
+    const int c_first = ((warp - 2) / 4) * Q::kDecChunks;
     uint32_t it = 0;
     bool ok = true;
     const float* bs32 = static_cast<const float*>(scales);
@@ -267,8 +277,8 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
       for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
         const int s = it % Q::kStages;
         const uint32_t ph = (it / Q::kStages) & 1u;
-        const int a = it & 1;
-        const uint32_t aph = (it >> 1) & 1u;
+        const int a = it % kABufs;
+        const uint32_t aph = (it / kABufs) & 1u;
         // multipliers for the four 32-wide K groups of this block
         uint32_t mul[4];
         if (ue8m0) {
@@ -288,12 +298,14 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
           ok = false;
           break;
         }
-        // 128 codes of this row, 16 per 16-byte chunk; chunk c sits at
-        // position c ^ (row & 7) of the 128-byte swizzled row.
+        // This warp's codes of the row (all 128, or one 64-wide half), 16 per
+        // 16-byte chunk; chunk c sits at position c ^ (row & 7) of the
+        // 128-byte swizzled row.
         const uint8_t* wrow = smem + size_t(s) * Q::kStageBytes + row * 128;
-        uint4 raw[8];
+        uint4 raw[Q::kDecChunks];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(wrow + ((c ^ (row & 7)) << 4));
+        for (int c = 0; c < Q::kDecChunks; ++c)
+          raw[c] = *reinterpret_cast<const uint4*>(wrow + (((c + c_first) ^ (row & 7)) << 4));
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         const bool got_a = __all_sync(0xffffffffu, mbar_wait(&aempty[a], aph ^ 1u, abort_flag));
@@ -303,17 +315,19 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_a + (uint32_t(quarter * 32) << 16) + uint32_t(a * kACols);
+        const uint32_t taddr = tmem_a + (uint32_t(quarter * 32) << 16) + uint32_t(a * kACols + c_first * 8);
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {            // 32 codes -> 16 TMEM columns
+        for (int h = 0; h < Q::kDecChunks / 2; ++h) {   // 32 codes -> 16 TMEM columns
           uint32_t words[16];
+          // group of 32 codes: h (first half or whole block) or h + 2 (second half)
+          const uint32_t m = c_first == 0 ? mul[h] : mul[(h + 2) & 3];
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
             const uint4 v = raw[2 * h + c2];
-            decode4_e4m3_bf16(v.x, mul[h], words[8 * c2 + 0], words[8 * c2 + 1]);
-            decode4_e4m3_bf16(v.y, mul[h], words[8 * c2 + 2], words[8 * c2 + 3]);
-            decode4_e4m3_bf16(v.z, mul[h], words[8 * c2 + 4], words[8 * c2 + 5]);
-            decode4_e4m3_bf16(v.w, mul[h], words[8 * c2 + 6], words[8 * c2 + 7]);
+            decode4_e4m3_bf16(v.x, m, words[8 * c2 + 0], words[8 * c2 + 1]);
+            decode4_e4m3_bf16(v.y, m, words[8 * c2 + 2], words[8 * c2 + 3]);
+            decode4_e4m3_bf16(v.z, m, words[8 * c2 + 4], words[8 * c2 + 5]);
+            decode4_e4m3_bf16(v.w, m, words[8 * c2 + 6], words[8 * c2 + 7]);
           }
           tmem_st_x16(taddr + uint32_t(h * 16), words);
         }
@@ -337,8 +351,8 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
       for (int j = 0; j < EC; ++j) acc[j] = 0.f;
       const int kb_stop = ue8m0 ? kb_begin + 1 : kb_end;   // UE8M0: one drain per tile
       for (int kb = kb_begin; kb < kb_stop; ++kb, ++acc_it) {
-        const int d = acc_it & 1;
-        const uint32_t dph = (acc_it >> 1) & 1u;
+        const int d = acc_it % Q::kDBufs;
+        const uint32_t dph = (acc_it / Q::kDBufs) & 1u;
         const float sc = ue8m0 ? 1.f : __ldg(bs32 + size_t(nt) * kblocks + kb);
         const bool got = __all_sync(0xffffffffu, mbar_wait(&dfull[d], dph, abort_flag));
         if (!got) {
@@ -366,27 +380,64 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
 
   __syncwarp();   // single-lane roles rejoin their warp before the aligned barriers below
   if (split > 1) {
-    const bool epi = warp >= 2 + kDecWarps;
-    float* red = reinterpret_cast<float*>(smem);   // [TM][BN] floats, reuses the stages
-    if (epi && rank != 0) {
+    // Rank 0 sums the ranks' partial tiles, in rank order, from distributed
+    // shared memory.
+    const bool epi = warp >= 2 + Q::kDecWarps;
+    if constexpr (TM < 128) {
+      // Each thread's columns are stored contiguously, so the remote reads
+      // are 16-byte vectors, four in flight.
+      float4* red = reinterpret_cast<float4*>(smem);   // [BN rows][TM / 4] float4, reuses the stages
+      if (epi && rank != 0) {
 #pragma unroll
-      for (int j = 0; j < EC; ++j) red[(col0 + j) * BN + row] = acc[j];
-    }
-    cluster_sync();
-    if (epi && rank == 0) {
-      for (int r = 1; r < split; ++r) {
-        const uint32_t base = map_shared_rank(smem_u32(red), uint32_t(r));
-#pragma unroll
-        for (int j = 0; j < EC; ++j) {
-          float v;
-          asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                       : "=f"(v)
-                       : "r"(base + uint32_t(((col0 + j) * BN + row) * 4))
-                       : "memory");
-          acc[j] += v;
-        }
+        for (int j4 = 0; j4 < EC / 4; ++j4)
+          red[row * (TM / 4) + col0 / 4 + j4] =
+              make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
       }
-      if (!*abort_flag) store_col<EC>(C, ldc, M, last_mt * TM + col0, last_nt * BN + row, acc);
+      cluster_sync();
+      if (epi && rank == 0) {
+        for (int r = 1; r < split; ++r) {
+          const uint32_t base =
+              map_shared_rank(smem_u32(red), uint32_t(r)) + uint32_t((row * (TM / 4) + col0 / 4) * 16);
+#pragma unroll
+          for (int g = 0; g < EC / 16; ++g) {
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = ld_dsmem_f4(base + uint32_t((4 * g + q) * 16));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int j = 16 * g + 4 * q;
+              acc[j] += v[q].x;
+              acc[j + 1] += v[q].y;
+              acc[j + 2] += v[q].z;
+              acc[j + 3] += v[q].w;
+            }
+          }
+        }
+        if (!*abort_flag) store_col<EC>(C, ldc, M, last_mt * TM + col0, last_nt * BN + row, acc);
+      }
+    } else {
+      // Widest tile (rarely split): scalar remote reads keep register use low.
+      float* red = reinterpret_cast<float*>(smem);   // [TM][BN] floats, reuses the stages
+      if (epi && rank != 0) {
+#pragma unroll
+        for (int j = 0; j < EC; ++j) red[(col0 + j) * BN + row] = acc[j];
+      }
+      cluster_sync();
+      if (epi && rank == 0) {
+        for (int r = 1; r < split; ++r) {
+          const uint32_t base = map_shared_rank(smem_u32(red), uint32_t(r));
+#pragma unroll
+          for (int j = 0; j < EC; ++j) {
+            float v;
+            asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                         : "=f"(v)
+                         : "r"(base + uint32_t(((col0 + j) * BN + row) * 4))
+                         : "memory");
+            acc[j] += v;
+          }
+        }
+        if (!*abort_flag) store_col<EC>(C, ldc, M, last_mt * TM + col0, last_nt * BN + row, acc);
+      }
     }
     cluster_sync();
   }

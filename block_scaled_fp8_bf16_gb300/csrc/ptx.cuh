@@ -327,6 +327,17 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
   return v;
 }
 
+// 16-byte load from distributed shared memory without a memory clobber, so
+// several can be in flight before their first use; they stay in program
+// order with the (volatile) cluster barrier and mapa before them.
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // ---------------------------------------------------------------- misc
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
