@@ -9,7 +9,7 @@ weights are rotated over enough copies that every step reads them from HBM
 
 One JSON line on stdout (rank 0).  `--sweep` additionally times every
 workload shape (W8A8 o_proj / prefill, W8A16 decode and UE8M0) with CUDA-graph
-replays over rotated weights and writes a table to gpurun_out/sweep.json.
+replays over rotated weights and writes the table as JSON to the given path.
 
 `--impl reference` times the float64 CPU oracle on a bounded row sample of the
 same workload (the oracle is the only reference implementation there is).
@@ -37,6 +37,24 @@ METRIC = "block-FP8 GEMM TFLOP/s (M≥256), weight GB/s (M≤16); % of GB300 roo
 HEAD_M, HEAD_N, HEAD_K = 4096, 4096, 4096
 WORKLOAD = "W8A8 o_proj linear, N=K=4096, M=4096: act quant (1x128) + block-scaled GEMM"
 FP8_PER_BF16 = 2.0       # nominal dense fp8 : bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+# DRAM traffic of one w8a8_pair_kernel launch at M = N = K = 4096, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only for
+# the kernel source it was taken on: reported as null once that file changes.
+TRAFFIC_CAPTURE = {"source": "block_scaled_fp8_bf16_gb300/csrc/gemm_w8a8_pair.cu",
+                   "md5": "22df028a10909e050ec2f4d6210ebd60",
+                   "bytes": 34_239_232 + 679_424}
+
+
+def measured_traffic():
+    import hashlib
+    path = os.path.join(ROOT, TRAFFIC_CAPTURE["source"])
+    try:
+        with open(path, "rb") as f:
+            digest = hashlib.md5(f.read()).hexdigest()
+    except OSError:
+        return None
+    return TRAFFIC_CAPTURE["bytes"] if digest == TRAFFIC_CAPTURE["md5"] else None
 
 
 def peaks():
@@ -284,11 +302,13 @@ def gpu_arm(args, world, rank, local):
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K,
                    "l2": f"inputs rotated over {R} copies ({R * per_copy / 2**20:.0f} MiB > 2x L2 {l2 / 2**20:.0f} MiB)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "kernel": "w8a8_kernel (block-scaled e4m3 GEMM)",
+        "roofline": {"bound": "tensor", "kernel": "w8a8_pair_kernel (block-scaled e4m3 GEMM, CTA pairs)",
                      "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / fp8_peak, 4),
                      "peak_note": f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x {FP8_PER_BF16} (nominal fp8:bf16)",
-                     "gemm_us": round(gemm_ms * 1e3, 2), "traffic": None},
+                     "gemm_us": round(gemm_ms * 1e3, 2), "traffic": measured_traffic(),
+                     "traffic_note": "DRAM bytes per launch from one ncu capture of this kernel source; "
+                                     "algorithmic reads A+As+B+Bs = 34.08 MB, C stays in L2"},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2, "steps": e2e_steps},
         "gpu_launches": 2 * args.steps,
@@ -510,7 +530,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--sweep", action="store_true", help="also time every workload shape")
+    ap.add_argument("--sweep", default=None, metavar="OUT.json",
+                    help="also time every workload shape and write the table to OUT.json")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None, help="run one configuration untimed (w8a8:M,N,K | quant:M,K | "
                                                   "w8a16:M,N,K,fmt) for profiling")
@@ -537,8 +558,8 @@ def main():
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline()
         if args.sweep:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            sweep(os.path.join(ROOT, "gpurun_out", "sweep.json"))
+            os.makedirs(os.path.dirname(os.path.abspath(args.sweep)), exist_ok=True)
+            sweep(args.sweep)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
