@@ -438,18 +438,22 @@ def sweep(out_path):
     for M in (256, 2048, 8192):
         for N, K in ((7168, 2048), (2048, 7168), (18432, 7168), (7168, 18432)):
             w8a8.append((M, N, K))
+    PDL = fp8blk.FLAG_PDL
     for M, N, K in w8a8:
         per = M * K * 3 + N * K + M * N * 2
         R = _rot_copies(per, l2, cap=32)
         sets = build_w8a8_set(M, N, K, R, outliers=(N == 4096 and K == 4096))
-        calls = [lambda s=s: fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"]) for s in sets]
         for s in sets:
             fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"])
         byt = M * K + (K // 128) * M * 4 + N * K + (N // 128) * (K // 128) * 4 + 2 * M * N
-        record("w8a8_gemm", M, N, K, graph_time(calls), 2.0 * M * N * K, byt, fp8_peak)
-        calls2 = [lambda s=s: (fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"]),
-                               fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"])) for s in sets]
-        record("w8a8_linear", M, N, K, graph_time(calls2), 2.0 * M * N * K, byt + 2 * M * K, fp8_peak)
+        for flags, tag in ((0, ""), (PDL, "_pdl")):
+            calls = [lambda s=s, f=flags: fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"], flags=f)
+                     for s in sets]
+            record("w8a8_gemm" + tag, M, N, K, graph_time(calls), 2.0 * M * N * K, byt, fp8_peak)
+            calls2 = [lambda s=s, f=flags: (fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"]),
+                                            fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"],
+                                                                    flags=f)) for s in sets]
+            record("w8a8_linear" + tag, M, N, K, graph_time(calls2), 2.0 * M * N * K, byt + 2 * M * K, fp8_peak)
         qcalls = [lambda s=s: fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"]) for s in sets]
         record("quant_act", M, 0, K, graph_time(qcalls), 0.0, 3 * M * K + (K // 128) * M * 4, fp8_peak)
         del sets
@@ -473,11 +477,12 @@ def sweep(out_path):
         sets = [(x.clone(), b.clone(), bs.clone(), torch.empty((M, N), dtype=torch.bfloat16, device="cuda"))
                 for _ in range(R)]
         fn = fp8blk.fp8blk_gemv_w8a16 if M <= 16 else fp8blk.fp8blk_gemm_w8a16
-        calls = [lambda s=s: fn(s[0], s[1], s[2], fmt, s[3]) for s in sets]
         sc_bytes = (N // 128) * (K // 128) * 4 if fmt == 0 else (N // 32) * (K // 32)
         byt = N * K + sc_bytes + M * K * 2 + M * N * 2
-        record("w8a16_f32" if fmt == 0 else "w8a16_ue8m0", M, N, K, graph_time(calls), 2.0 * M * N * K, byt,
-               pk["bf16"])
+        for flags, tag in ((0, ""), (PDL, "_pdl")):
+            calls = [lambda s=s, f=flags: fn(s[0], s[1], s[2], fmt, s[3], flags=f) for s in sets]
+            record(("w8a16_f32" if fmt == 0 else "w8a16_ue8m0") + tag, M, N, K, graph_time(calls),
+                   2.0 * M * N * K, byt, pk["bf16"])
         del sets
         torch.cuda.empty_cache()
     with open(out_path, "w") as f:

@@ -21,6 +21,9 @@ LIB_PATH = os.path.join(_HERE, "libfp8blk.so")
 SCALE_F32_128x128 = 0
 SCALE_UE8M0_32x32 = 1
 
+# Launch flags of the GEMM entry points (FP8BLK_FLAG_* in the header).
+FLAG_PDL = 1
+
 STATUS_NAMES = {
     0: "FP8BLK_OK",
     1: "FP8BLK_ERR_INVALID_ARG",
@@ -37,11 +40,12 @@ STATUS_NAMES = {
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _I32 = ctypes.c_int32
+_U32 = ctypes.c_uint32
 EXPORTS = {
     "fp8blk_quant_act": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
-    "fp8blk_gemm_w8a8": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P]),
-    "fp8blk_gemm_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _P]),
-    "fp8blk_gemv_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _P]),
+    "fp8blk_gemm_w8a8": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _U32, _P]),
+    "fp8blk_gemm_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _U32, _P]),
+    "fp8blk_gemv_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_quant_weight": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "fp8blk_validate_weights": (_I32, [_P, _I64, _P, _I32, _I64, _I64, _P, _P]),
     "fp8blk_debug_decode_e4m3": (_I32, [_P, _I64, _I32, _P, _P]),
@@ -139,31 +143,31 @@ def fp8blk_quant_act(x, a, a_scales, stream=None):
                                 _stream(stream)), "fp8blk_quant_act")
 
 
-def fp8blk_gemm_w8a8(a, a_scales, b, b_scales, c, stream=None):
+def fp8blk_gemm_w8a8(a, a_scales, b, b_scales, c, stream=None, flags=0):
     """C[M, N] bf16 = block-scaled a[M, K] e4m3 x b[N, K] e4m3."""
     a, b = _bytes_tensor(a), _bytes_tensor(b)
     M, K = a.shape
     N = b.shape[0]
     _check(_L().fp8blk_gemm_w8a8(_ptr(a), _ld(a), _ptr(a_scales), _ld(a_scales), _ptr(b), _ld(b), _ptr(b_scales),
-                                _ptr(c), _ld(c), M, N, K, _stream(stream)), "fp8blk_gemm_w8a8")
+                                _ptr(c), _ld(c), M, N, K, int(flags), _stream(stream)), "fp8blk_gemm_w8a8")
 
 
-def fp8blk_gemm_w8a16(x, b, b_scales, fmt, c, stream=None):
+def fp8blk_gemm_w8a16(x, b, b_scales, fmt, c, stream=None, flags=0):
     """C[M, N] bf16 = x[M, K] bf16 x b[N, K] e4m3 with fp32 128x128 or UE8M0 32x32 scales."""
     b = _bytes_tensor(b)
     M, K = x.shape
     N = b.shape[0]
     _check(_L().fp8blk_gemm_w8a16(_ptr(x), _ld(x), _ptr(b), _ld(b), _ptr(b_scales), int(fmt), _ptr(c), _ld(c),
-                                 M, N, K, _stream(stream)), "fp8blk_gemm_w8a16")
+                                 M, N, K, int(flags), _stream(stream)), "fp8blk_gemm_w8a16")
 
 
-def fp8blk_gemv_w8a16(x, b, b_scales, fmt, c, stream=None):
+def fp8blk_gemv_w8a16(x, b, b_scales, fmt, c, stream=None, flags=0):
     """Decode-size (M <= 16) form of fp8blk_gemm_w8a16."""
     b = _bytes_tensor(b)
     M, K = x.shape
     N = b.shape[0]
     _check(_L().fp8blk_gemv_w8a16(_ptr(x), _ld(x), _ptr(b), _ld(b), _ptr(b_scales), int(fmt), _ptr(c), _ld(c),
-                                 M, N, K, _stream(stream)), "fp8blk_gemv_w8a16")
+                                 M, N, K, int(flags), _stream(stream)), "fp8blk_gemv_w8a16")
 
 
 def fp8blk_quant_weight(w, b, b_scales, stream=None):
@@ -225,27 +229,27 @@ def quant_weight(w, stream=None):
     return b, s
 
 
-def gemm_w8a8(a, a_scales, b, b_scales, out=None, stream=None):
+def gemm_w8a8(a, a_scales, b, b_scales, out=None, stream=None, flags=0):
     import torch
     if out is None:
         out = torch.empty((a.shape[0], b.shape[0]), dtype=torch.bfloat16, device=a.device)
-    fp8blk_gemm_w8a8(a, a_scales, b, b_scales, out, stream)
+    fp8blk_gemm_w8a8(a, a_scales, b, b_scales, out, stream, flags)
     return out
 
 
-def gemm_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None):
+def gemm_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None, flags=0):
     import torch
     if out is None:
         out = torch.empty((x.shape[0], b.shape[0]), dtype=torch.bfloat16, device=x.device)
-    fp8blk_gemm_w8a16(x, b, b_scales, fmt, out, stream)
+    fp8blk_gemm_w8a16(x, b, b_scales, fmt, out, stream, flags)
     return out
 
 
-def gemv_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None):
+def gemv_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None, flags=0):
     import torch
     if out is None:
         out = torch.empty((x.shape[0], b.shape[0]), dtype=torch.bfloat16, device=x.device)
-    fp8blk_gemv_w8a16(x, b, b_scales, fmt, out, stream)
+    fp8blk_gemv_w8a16(x, b, b_scales, fmt, out, stream, flags)
     return out
 
 

@@ -150,6 +150,8 @@ fp8blk_status make_map(CUtensorMap& out, CUtensorMapDataType dtype, const void* 
 
 // ------------------------------------------------------------------ checks
 
+constexpr uint32_t kKnownFlags = FP8BLK_FLAG_PDL;
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline fp8blk_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8BLK_OK : FP8BLK_ERR_CUDA; }
@@ -176,11 +178,13 @@ fp8blk_status zero_output(void* c, int64_t ldc, int64_t M, int64_t N, cudaStream
 }
 
 fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, const void* sc, int fmt, void* c,
-                        int64_t ldc, int64_t M, int64_t N, int64_t K, int tile_m, cudaStream_t s) {
+                        int64_t ldc, int64_t M, int64_t N, int64_t K, uint32_t flags, cudaStream_t s) {
   DeviceInfo dev;
   fp8blk_status st = device_info(dev);
   if (st != FP8BLK_OK) return st;
   if (K == 0) return zero_output(c, ldc, M, N, s);
+  const bool decode = M <= kW8A16DecodeMaxM;
+  const int tile_m = decode ? (M <= 16 ? 16 : 32) : w8a16_pick_tile_m(M);
   GemmW8A16Args p;
   st = make_map(p.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, uint64_t(K), uint64_t(N), uint64_t(ldb), 128, 128);
   if (st != FP8BLK_OK) return st;
@@ -195,8 +199,9 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   p.N = int(N);
   p.K = int(K);
   p.tile_m = tile_m;
+  p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
   p.err = dev.err_word;
-  return cuda_status(launch_gemm_w8a16(p, dev, s));
+  return cuda_status(decode ? launch_w8a16_decode(p, dev, s) : launch_gemm_w8a16(p, dev, s));
 }
 
 }  // namespace
@@ -224,8 +229,8 @@ fp8blk_status fp8blk_quant_act(const void* x_bf16, int64_t M, int64_t K, int64_t
 
 fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda, const float* a_scales, int64_t lds,
                                const void* b_e4m3, int64_t ldb, const float* b_scales, void* c_bf16, int64_t ldc,
-                               int64_t M, int64_t N, int64_t K, fp8blk_stream_t stream) {
-  if (M < 0 || N < 0 || K < 0) return FP8BLK_ERR_INVALID_ARG;
+                               int64_t M, int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || (flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
   if (M > kIntMax || N > kIntMax || K > kIntMax) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
   if (M == 0 || N == 0) return FP8BLK_OK;
@@ -259,27 +264,30 @@ fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda, const float* a_s
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
+  p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
   p.err = dev.err_word;
   return cuda_status(launch_gemm_w8a8(p, dev, s));
 }
 
 fp8blk_status fp8blk_gemm_w8a16(const void* x_bf16, int64_t ldx, const void* b_e4m3, int64_t ldb,
                                 const void* b_scales, fp8blk_scale_fmt fmt, void* c_bf16, int64_t ldc, int64_t M,
-                                int64_t N, int64_t K, fp8blk_stream_t stream) {
+                                int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
+  if ((flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
   fp8blk_status st = check_w8a16_args(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K);
   if (st != FP8BLK_OK || M == 0 || N == 0) return st;
-  return run_w8a16(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K, w8a16_pick_tile_m(M),
+  return run_w8a16(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K, flags,
                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 fp8blk_status fp8blk_gemv_w8a16(const void* x_bf16, int64_t ldx, const void* b_e4m3, int64_t ldb,
                                 const void* b_scales, fp8blk_scale_fmt fmt, void* c_bf16, int64_t ldc, int64_t M,
-                                int64_t N, int64_t K, fp8blk_stream_t stream) {
+                                int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
+  if ((flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
   fp8blk_status st = check_w8a16_args(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K);
   if (st != FP8BLK_OK) return st;
   if (M > 16) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
   if (M == 0 || N == 0) return FP8BLK_OK;
-  return run_w8a16(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K, 16,
+  return run_w8a16(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K, flags,
                    reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
+  griddep_launch_dependents();   // the next kernel may start its prologue; it gets an SM when this CTA leaves
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_tiles = N / BN;
@@ -181,6 +183,7 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      griddep_wait();   // activations may come from the previous kernel (programmatic dependent launch)
       uint32_t it = 0;
       bool ok = true;
       const uint64_t pol_w = m_tiles > 1 ? policy_evict_last() : policy_evict_first();
@@ -339,6 +342,7 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue
+    griddep_wait();   // the output may still be read or written by the previous kernel
     uint32_t acc_it = 0;
     bool ok = true;
     const float* bs32 = static_cast<const float*>(scales);
@@ -482,13 +486,15 @@ cudaError_t launch_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_
   cfg.blockDim = dim3(Q::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Q::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(split);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, w8a16_kernel<TM>, p.tmW, p.tmX, p.scales, p.fmt,
                             static_cast<__nv_bfloat16*>(p.C), p.ldc, p.M, p.N, p.K, split, p.err);
 }

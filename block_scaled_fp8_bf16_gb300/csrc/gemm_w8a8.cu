@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
+  griddep_launch_dependents();   // the next kernel may start its prologue; it gets an SM when this CTA leaves
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int m_tiles = (M + BM - 1) / BM;
@@ -165,34 +167,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t it = 0;
-      bool ok = true;
+      // Items are this CTA's (tile, K block) pairs in order.
+      const int nkb = kb_end - kb_begin;
+      const int my_tiles = cluster_id < num_tiles ? (num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0;
+      const int n_items = my_tiles * nkb;
       // Weights are re-read by every row tile when there are several; with a
       // single row tile they stream through once.
       const uint64_t pol_b = m_tiles > 1 ? policy_evict_last() : policy_evict_first();
-      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      // Under programmatic dependent launch the weight tiles of the first
+      // stages are requested before the previous kernel has finished; the
+      // activations and their scales only after it.
+      const int pre = n_items < kStages ? n_items : kStages;
+      for (int it = 0; it < pre; ++it) {
         int mt, nt;
-        tile_coords(t, m_tiles, n_tiles, mt, nt);
-        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
-            raise_error(err, abort_flag, kSiteProducerEmpty);
-            ok = false;
-            break;
-          }
-          uint8_t* sa = smem + size_t(s) * kStageBytes;
-          uint8_t* sb = sa + kStageA;
-          mbar_arrive_expect_tx(&full[s], kStageBytes + kStageAs);
-          tma_load_2d(sa, &tmA, &full[s], kb * BK, mt * BM);
-          tma_load_2d_hint(sb, &tmB, &full[s], kb * BK, nt * BN, pol_b);
-          tma_load_2d(as_stage + s * BM, &tmAs, &full[s], mt * BM, kb);
-        }
+        tile_coords(cluster_id + (it / nkb) * num_clusters, m_tiles, n_tiles, mt, nt);
+        const int kb = kb_begin + it % nkb;
+        mbar_arrive_expect_tx(&full[it], kStageBytes + kStageAs);
+        tma_load_2d_hint(smem + size_t(it) * kStageBytes + kStageA, &tmB, &full[it], kb * BK, nt * BN, pol_b);
       }
-      if (!ok) {
+      griddep_wait();
+      for (int it = 0; it < pre; ++it) {
+        int mt, nt;
+        tile_coords(cluster_id + (it / nkb) * num_clusters, m_tiles, n_tiles, mt, nt);
+        const int kb = kb_begin + it % nkb;
+        tma_load_2d(smem + size_t(it) * kStageBytes, &tmA, &full[it], kb * BK, mt * BM);
+        tma_load_2d(as_stage + it * BM, &tmAs, &full[it], mt * BM, kb);
+      }
+      int it = pre;
+      for (; it < n_items; ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (uint32_t(it) / kStages) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
+          raise_error(err, abort_flag, kSiteProducerEmpty);
+          break;
+        }
+        int mt, nt;
+        tile_coords(cluster_id + (it / nkb) * num_clusters, m_tiles, n_tiles, mt, nt);
+        const int kb = kb_begin + it % nkb;
+        uint8_t* sa = smem + size_t(s) * kStageBytes;
+        uint8_t* sb = sa + kStageA;
+        mbar_arrive_expect_tx(&full[s], kStageBytes + kStageAs);
+        tma_load_2d(sa, &tmA, &full[s], kb * BK, mt * BM);
+        tma_load_2d_hint(sb, &tmB, &full[s], kb * BK, nt * BN, pol_b);
+        tma_load_2d(as_stage + s * BM, &tmAs, &full[s], mt * BM, kb);
+      }
+      if (it < n_items) {
         // Let every copy this thread issued land before the CTA can exit.
-        const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0u;
-        for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1u, nullptr);
+        const int first = it > kStages ? it - kStages : 0;
+        for (int j = first; j < it; ++j) mbar_wait(&full[j % kStages], (uint32_t(j) / kStages) & 1u, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -235,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue
+    griddep_wait();        // the output may still be read or written by the previous kernel
     uint32_t it = 0;       // stage counter, in step with the producer and the MMA issuer
     bool ok = true;
     for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
@@ -370,13 +393,15 @@ cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaS
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(split);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, w8a8_kernel, p.tmA, p.tmB, p.tmAs, p.Bs,
                             static_cast<__nv_bfloat16*>(p.C), p.ldc, p.M, p.N, p.K, split, p.err);
 }

@@ -134,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
+  griddep_launch_dependents();   // the next kernel may start its prologue; it gets an SM when this CTA leaves
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = static_cast<int>(cluster_ctarank());
@@ -184,6 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool a_side = warp == 0;
     const uint32_t full0_base = map_shared_rank(smem_u32(full), 0);
     if (lane == 0) {
+      // Under programmatic dependent launch the weights stream in at once;
+      // the activations and their scales wait for the previous kernel.
+      if (a_side) griddep_wait();
       uint32_t it = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
@@ -276,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = (e >> 2) * kCols;
     const int row = quarter * 32 + lane;
     const uint32_t dempty0 = map_shared_rank(smem_u32(dempty), 0);
+    griddep_wait();   // the output may still be read or written by the previous kernel
     float2 acc[kCols / 2];
     uint32_t it = 0;
     bool ok = true;
@@ -378,13 +384,15 @@ cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, 
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel, p.tmA, p.tmB, p.tmAs, p.Bs, static_cast<__nv_bfloat16*>(p.C),
                             p.ldc, p.M, p.N, p.K, p.err);
 }

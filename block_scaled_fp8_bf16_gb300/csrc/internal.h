@@ -14,6 +14,7 @@ enum DeviceErr : int {
   kDevErrNone = 0,
   kDevErrW8A8 = 0x100,
   kDevErrW8A16 = 0x200,
+  kDevErrW8A16Decode = 0x300,
 };
 enum WaitSite : int {
   kSiteProducerEmpty = 1,
@@ -24,6 +25,8 @@ enum WaitSite : int {
   kSiteDecodeAEmpty = 6,
   kSiteMmaAFull = 7,
   kSiteDrain = 8,
+  kSiteReduceEmpty = 9,
+  kSiteReduceFull = 10,
 };
 
 struct DeviceInfo {
@@ -75,6 +78,7 @@ struct GemmW8A8Args {
   void* C;            // bf16 [M, ldc]
   int64_t ldc;
   int M, N, K;
+  bool pdl;           // launch with programmatic stream serialisation
   int* err;
 };
 constexpr int kW8A8TileM = 128;
@@ -95,11 +99,45 @@ struct GemmW8A16Args {
   int64_t ldc;
   int M, N, K;
   int tile_m;         // token tile (MMA N): 16, 32, 64 or 128
+  bool pdl;           // launch with programmatic stream serialisation
   int* err;
 };
 constexpr int kW8A16TileN = 128;
 constexpr int kW8A16MaxTileM = 128;
 int w8a16_pick_tile_m(int64_t M);
 cudaError_t launch_gemm_w8a16(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t s);
+
+// Decode-size W8A16 (M <= tile_m, tile_m 16 or 32).
+constexpr int kW8A16DecodeMaxM = 32;
+cudaError_t launch_w8a16_decode(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t s);
+
+// Work split of the decode kernel: K is divided over clusters of `split`
+// CTAs (1, 2, 4 or 8) and the 128-row weight tiles run persistently over
+// `clusters` clusters.  Chosen to minimise the per-CTA K blocks on the
+// critical path, rounds x ceil(K blocks / split), with half a block charged
+// per round for the cross-CTA reduction; max_clusters(s) is how many
+// clusters of s CTAs can be resident at once.
+struct W8A16DecodePlan {
+  int split;
+  int clusters;
+};
+template <class MaxClusters>
+W8A16DecodePlan w8a16_decode_plan(int N, int K, int num_sms, MaxClusters max_clusters) {
+  const int n_tiles = N / kW8A16TileN;
+  const int kblocks = K / 128;
+  W8A16DecodePlan best{1, n_tiles < num_sms ? n_tiles : num_sms};
+  long long best_cost = 2LL * ((n_tiles + num_sms - 1) / num_sms) * kblocks;
+  for (int s = 2; s <= kMaxSplitK && s <= kblocks; s *= 2) {
+    const int c = max_clusters(s);
+    if (c <= 0) continue;
+    const long long rounds = (n_tiles + c - 1) / c;
+    const long long cost = rounds * (2LL * ((kblocks + s - 1) / s) + 1);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = W8A16DecodePlan{s, n_tiles < c ? n_tiles : c};
+    }
+  }
+  return best;
+}
 
 }  // namespace fp8blk

@@ -99,6 +99,10 @@ constexpr int kQuantRows = 4;
 __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
                                                         int64_t ldx, uint8_t* __restrict__ a, int64_t lda,
                                                         float* __restrict__ scales, int64_t lds) {
+  // A GEMM launched after this kernel with programmatic dependent launch may
+  // begin streaming its weights now; it waits for this grid before reading
+  // the codes and scales written here.
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int hl = lane & 15;
   const int64_t g = int64_t(blockIdx.y) * 2 + (lane >> 4);

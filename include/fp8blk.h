@@ -89,7 +89,24 @@ typedef struct {
   int32_t max_split_k;        /* largest split-K cluster the kernels use */
 } fp8blk_constraints;
 
-#define FP8BLK_ABI_VERSION 1
+#define FP8BLK_ABI_VERSION 2
+
+/*
+ * Launch flags of the three GEMM entry points (bitwise OR; 0 = none).
+ *
+ * FP8BLK_FLAG_PDL  programmatic dependent launch.  The call's kernel may
+ *   start while kernels queued before it on the stream are still running:
+ *   it sets up, then reads the weights (b_e4m3) and their scales (b_scales)
+ *   at once, and reads the activations and their scales, and writes the
+ *   output, only after those kernels have finished and their writes are
+ *   visible.  This hides the launch and the first weight fetch behind the
+ *   previous kernel's tail, which matters when one call streams only a few
+ *   megabytes (decode).  Set it only when no kernel that may still be
+ *   running at that point writes the weights or their scales (the usual
+ *   case: weights prepared once, long before).  Without the flag every
+ *   call waits for the previous work on the stream as usual.
+ */
+#define FP8BLK_FLAG_PDL 1u
 
 /* ------------------------------------------------------------------------ */
 /* Hot path                                                                 */
@@ -132,6 +149,7 @@ FP8BLK_API fp8blk_status fp8blk_quant_act(const void* x_bf16, int64_t M, int64_t
  *  c_bf16    [M, N] bf16 out, row pitch ldc elements (ldc*2 % 16 == 0).
  *  N % 128 == 0, K % 128 == 0, M >= 0 (M == 0 is a no-op).
  *  Weights are assumed finite (see fp8blk_validate_weights).
+ *  flags     FP8BLK_FLAG_* (unknown bits: FP8BLK_ERR_INVALID_ARG).
  */
 FP8BLK_API fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda,
                                const float* a_scales, int64_t lds,
@@ -139,7 +157,7 @@ FP8BLK_API fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda,
                                const float* b_scales,
                                void* c_bf16, int64_t ldc,
                                int64_t M, int64_t N, int64_t K,
-                               fp8blk_stream_t stream);
+                               uint32_t flags, fp8blk_stream_t stream);
 
 /*
  * W8A16 GEMM: bf16 activations, e4m3 weights decoded to bf16 in registers by
@@ -160,16 +178,20 @@ FP8BLK_API fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda,
  *  b_e4m3  [N, K] e4m3, row pitch ldb bytes (ldb % 16 == 0).
  *  c_bf16  [M, N] bf16 out, row pitch ldc elements.
  *  M == 0 is a no-op.  Scales outside [-14, 7] are outside the contract.
+ *  flags   FP8BLK_FLAG_* (unknown bits: FP8BLK_ERR_INVALID_ARG).
+ *  M <= 32 runs the decode-size kernel (weight stream split over clusters of
+ *  CTAs); larger M the token-tiled kernel.
  */
 FP8BLK_API fp8blk_status fp8blk_gemm_w8a16(const void* x_bf16, int64_t ldx,
                                 const void* b_e4m3, int64_t ldb,
                                 const void* b_scales, fp8blk_scale_fmt fmt,
                                 void* c_bf16, int64_t ldc,
                                 int64_t M, int64_t N, int64_t K,
-                                fp8blk_stream_t stream);
+                                uint32_t flags, fp8blk_stream_t stream);
 
 /*
- * Decode-size W8A16 product (M <= 16), same contract as fp8blk_gemm_w8a16.
+ * Decode-size W8A16 product (M <= 16), same contract as fp8blk_gemm_w8a16
+ * (it runs the same decode-size kernel as fp8blk_gemm_w8a16 at M <= 16).
  * The weights are streamed once from HBM ("FP8 / NVFP4 weight-only
  * inference ...", section 4.3: at small M the time is set by DRAM
  * bandwidth).  M > 16 returns FP8BLK_ERR_UNSUPPORTED_SHAPE.
@@ -179,7 +201,7 @@ FP8BLK_API fp8blk_status fp8blk_gemv_w8a16(const void* x_bf16, int64_t ldx,
                                 const void* b_scales, fp8blk_scale_fmt fmt,
                                 void* c_bf16, int64_t ldc,
                                 int64_t M, int64_t N, int64_t K,
-                                fp8blk_stream_t stream);
+                                uint32_t flags, fp8blk_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Off the hot path                                                          */

@@ -39,6 +39,22 @@ def test_library_exports_every_declared_symbol(fp8blk):
     assert set(declared_symbols()) == set(fp8blk.EXPORTS)
 
 
+def declared_arg_counts():
+    text = open(HEADER).read()
+    out = {}
+    for m in re.finditer(r"FP8BLK_API\s+[\w\s\*]+?\b(fp8blk_\w+)\s*\(([^)]*)\)", text):
+        params = [p for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        out[m.group(1)] = len(params)
+    return out
+
+
+def test_binding_arg_counts_match_header(fp8blk):
+    counts = declared_arg_counts()
+    assert set(counts) == set(fp8blk.EXPORTS)
+    for name, n in counts.items():
+        assert len(fp8blk.EXPORTS[name][1]) == n, name
+
+
 def test_no_other_dynamic_exports(fp8blk):
     out = subprocess.run(["nm", "-D", "--defined-only", fp8blk.LIB_PATH], capture_output=True, text=True).stdout
     ours = {l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("fp8blk")}
@@ -52,7 +68,7 @@ def test_no_cuda_driver_link_dependency(fp8blk):
 
 def test_constraints(fp8blk):
     c = fp8blk.fp8blk_query_constraints()
-    assert c["abi_version"] == 1
+    assert c["abi_version"] == 2
     assert c["scale_block_k"] == 128 and c["scale_block_n"] == 128 and c["ue8m0_block"] == 32
     assert c["gemv_max_m"] == 16 and c["ptr_align_bytes"] == 16 and c["lds_multiple"] == 4
 
@@ -67,8 +83,8 @@ P = 1 << 20          # a 16-byte aligned fake pointer; never dereferenced
 MIS = P + 4          # misaligned fake pointer
 
 
-def call_w8a8(lib, a=P, lda=512, s=P, lds=16, b=P, ldb=512, bs=P, c=P, ldc=256, M=16, N=256, K=512):
-    return lib.fp8blk_gemm_w8a8(a, lda, s, lds, b, ldb, bs, c, ldc, M, N, K, None)
+def call_w8a8(lib, a=P, lda=512, s=P, lds=16, b=P, ldb=512, bs=P, c=P, ldc=256, M=16, N=256, K=512, flags=0):
+    return lib.fp8blk_gemm_w8a8(a, lda, s, lds, b, ldb, bs, c, ldc, M, N, K, flags, None)
 
 
 def test_w8a8_argument_errors(fp8blk):
@@ -89,13 +105,15 @@ def test_w8a8_argument_errors(fp8blk):
     assert call_w8a8(lib, lds=18) == 3
     assert call_w8a8(lib, ldc=260) == 3
     assert call_w8a8(lib, M=1 << 31) == 2
+    assert call_w8a8(lib, flags=2) == 1             # unknown launch flag
+    assert call_w8a8(lib, M=0, flags=1) == 0        # FP8BLK_FLAG_PDL is known
 
 
 def test_w8a16_and_gemv_argument_errors(fp8blk):
     lib = fp8blk._L()
 
-    def g(fn, x=P, ldx=512, b=P, ldb=512, sc=P, fmt=0, c=P, ldc=256, M=4, N=256, K=512):
-        return getattr(lib, fn)(x, ldx, b, ldb, sc, fmt, c, ldc, M, N, K, None)
+    def g(fn, x=P, ldx=512, b=P, ldb=512, sc=P, fmt=0, c=P, ldc=256, M=4, N=256, K=512, flags=0):
+        return getattr(lib, fn)(x, ldx, b, ldb, sc, fmt, c, ldc, M, N, K, flags, None)
 
     for fn in ("fp8blk_gemm_w8a16", "fp8blk_gemv_w8a16"):
         assert g(fn, fmt=2) == 1
@@ -107,6 +125,8 @@ def test_w8a16_and_gemv_argument_errors(fp8blk):
         assert g(fn, x=MIS) == 3
         assert g(fn, ldx=516) == 3
         assert g(fn, ldb=520) == 3
+        assert g(fn, flags=4) == 1
+        assert g(fn, M=0, flags=1) == 0
     assert g("fp8blk_gemv_w8a16", M=17) == 2
 
 
