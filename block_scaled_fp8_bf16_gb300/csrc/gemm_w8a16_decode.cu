@@ -39,8 +39,9 @@
 //                 its first loads go out before the CTA-wide setup barrier.
 //   warp 1        TMA producer of the bf16 token tiles [TM x 128 k].
 //   warps 2, 3    MMA issuers (lane 0); warp 2 also owns the TMEM allocation.
-//   decode warps  8: two per TMEM lane quarter, each decodes 64 codes of its
-//                 row per K block into a TMEM A buffer.
+//   decode warps  8, in two groups of four (one warp per TMEM lane quarter);
+//                 group g decodes whole rows of every other K block into a
+//                 TMEM A buffer, the blocks MMA issuer g multiplies.
 //   4 warps       promotion + epilogue: thread = weight row, TM accumulators.
 #include <cuda_bf16.h>
 
@@ -60,20 +61,23 @@ constexpr int kEpiWarps = 4;
 constexpr int kWarpXProducer = 1;
 constexpr int kWarpIssuer0 = 2;
 constexpr int kWarpDec0 = kWarpIssuer0 + kIssuers;
-constexpr int kXStages = 6;       // token tiles in flight
+constexpr int kXStages = 4;       // token tiles in flight
 constexpr int kABufs = 4;         // decoded A blocks in TMEM
 constexpr int kDBufs = 8;         // FP32 partials in TMEM
 constexpr int kRing = 8;          // MMA-completion barriers, indexed by K-block count
 constexpr int kBarrierBytes = 512;
+constexpr int kEarlyW = 4;        // weight stages requested before the setup barrier
 
 template <int TM>
 struct DecCfg {
-  static constexpr int kDecWarps = 8;
-  static constexpr int kDecChunks = 8 / (kDecWarps / 4);       // 16-byte chunks of a row per decode warp
+  // Decode warps form kIssuers groups of four (one per TMEM lane quarter);
+  // group g decodes whole rows of the K blocks it with it % kIssuers == g,
+  // the blocks issuer g multiplies.
+  static constexpr int kDecWarps = 4 * kIssuers;
   static constexpr int kWarpEpi0 = kWarpDec0 + kDecWarps;
   static constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
   static constexpr int kStageX = TM * BK * 2;
-  static constexpr int kWStages = TM == 16 ? 11 : 9;           // weight ring, as deep as shared memory allows
+  static constexpr int kWStages = TM == 16 ? 12 : 10;          // weight ring, as deep as shared memory allows
   static constexpr int kRedFloats = BN * TM;                   // one partial tile, token-major [TM][BN]
   static constexpr size_t kXOff = size_t(kWStages) * kStageW;
   static constexpr size_t kRedOff = kXOff + size_t(kXStages) * kStageX;
@@ -95,7 +99,9 @@ struct DecCfg {
   static_assert((2 * kWStages + kXStages + kABufs + kRing + kDBufs + 5) * 8 + 8 <= kBarrierBytes, "barrier area");
   static_assert(kXOff % 1024 == 0 && kRedOff % 1024 == 0, "swizzled tiles need 1024-B alignment");
   static_assert(kWarpDec0 % 4 == 0 && kDecWarps % 4 == 0, "warp w may only reach TMEM lanes 32*(w%4)..+31");
-  static_assert(kDecChunks % 2 == 0, "a decode warp covers whole 32-wide K groups");
+  // Each decode group consumes every use of the stages it owns (those with
+  // s % kIssuers == g), so its parity waits are never two phases behind.
+  static_assert(kWStages % kIssuers == 0, "weight stages split evenly between the decode groups");
 };
 
 __device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, int site) {
@@ -152,15 +158,17 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
   // Weight loads of the first ring stages: issued by the weight producer
   // (thread 0) right after it has set up the barriers, so that the first
   // DRAM round trip overlaps the TMEM allocation and the setup barrier.
+  // One thread issues a box about every 300 cycles, so only a few go out
+  // before the barrier; the producer loop issues the rest.
   const uint64_t pol_w = policy_evict_first();
-  const int pre = n_items < Q::kWStages ? n_items : Q::kWStages;
+  const int pre = n_items < kEarlyW ? n_items : kEarlyW;
   if (threadIdx.x == 0) {
     for (int s = 0; s < Q::kWStages; ++s) {
       mbar_init(&wfull[s], 1);
-      mbar_init(&wempty[s], Q::kDecWarps);
+      mbar_init(&wempty[s], 4);   // the four warps of one decode group
     }
     for (int j = 0; j < kXStages; ++j) mbar_init(&xfull[j], 1);
-    for (int i = 0; i < kABufs; ++i) mbar_init(&afull[i], Q::kDecWarps);
+    for (int i = 0; i < kABufs; ++i) mbar_init(&afull[i], 4);
     for (int i = 0; i < kRing; ++i) mbar_init(&mdone[i], 1);
     for (int i = 0; i < kDBufs; ++i) mbar_init(&dempty[i], kEpiWarps);
     for (int i = 0; i < 2; ++i) {
@@ -188,12 +196,13 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  if (split > 1) {
-    cluster_sync();   // peers' barriers are initialised before any remote arrive
-  } else {
-    __syncthreads();
-  }
+  __syncthreads();
   tc_fence_after();
+  if (split > 1) {
+    // Peers' barriers are initialised before any remote arrive reaches them.
+    cluster_arrive_relaxed();
+    cluster_wait();
+  }
   const uint32_t tmem = *tmem_holder;
   const uint32_t tmem_a = tmem;                               // kABufs x 64 columns of decoded weights
   const uint32_t tmem_d = tmem + uint32_t(kABufs * kACols);   // kDBufs x TM columns of FP32 partials
@@ -205,12 +214,12 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
     // Weights never depend on the previous kernel: no griddepcontrol.wait.
     if (lane == 0) {
       // Ring position and (tile, K block) of item `it`, advanced without
-      // divisions.  The loop runs only when the first pass filled the whole
-      // ring, so it starts at stage 0 waiting for the first release (phase 0).
-      int it = pre, s = 0, nt = cluster_id + (pre / nkb) * num_clusters, kb = kb_begin + pre % nkb;
-      uint32_t ph = 0;
+      // divisions.  Stage s is reused from item kWStages on, after its
+      // previous contents were released (wempty phase (it / kWStages - 1)).
+      int it = pre, s = pre, nt = cluster_id + (pre / nkb) * num_clusters, kb = kb_begin + pre % nkb;
+      uint32_t ph = 1;   // parity of the release to wait for, once the ring wraps
       for (; it < n_items; ++it) {
-        if (!mbar_wait_sleep(&wempty[s], ph, abort_flag)) {
+        if (it >= Q::kWStages && !mbar_wait_sleep(&wempty[s], ph, abort_flag)) {
           raise_error(err, abort_flag, kSiteProducerEmpty);
           break;
         }
@@ -288,28 +297,34 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
     }
   } else if (warp < Q::kWarpEpi0) {
     // ------------------------------------------------------------ decode
-    constexpr int NC = Q::kDecChunks;
-    constexpr int NG = NC / 2;                                     // 32-wide K groups per warp
-    const int c_first = ((warp - kWarpDec0) / 4) * NC;           // first 16-byte chunk of the row
+    // Group g decodes the K blocks it = g, g + kIssuers, ...: whole 128-code
+    // rows, one block per loop, so the two groups of a lane quarter run out
+    // of step with each other and each block pays one set of waits.
+    const int g = (warp - kWarpDec0) / 4;
     const uint32_t* ue32 = static_cast<const uint32_t*>(scales);
-    uint32_t ewin = 0;   // lane l: exponent bytes of K block (window base + l) for this warp's 32 rows
-    int s = 0, j = 0, nt = cluster_id;
+    uint32_t ewin = 0;   // lane l: exponent bytes of K block (win + l) of this tile, for this warp's 32 rows
+    int win = -32;
+    int s = g, j = g, nt = cluster_id;
+    while (j >= nkb) {
+      j -= nkb;
+      nt += num_clusters;
+    }
     uint32_t ph = 0;
-    for (int it = 0; it < n_items; ++it) {
+    for (int it = g; it < n_items; it += kIssuers) {
       const int a = it % kABufs;
-      uint32_t mul[NG];   // multipliers of this warp's 32-wide K groups
+      uint32_t mul[4];   // multipliers of the four 32-wide K groups of the block
       if (ue8m0) {
-        if ((j & 31) == 0) {
+        if (j < win || j >= win + 32) {
+          win = j;
           const int kb = kb_begin + j + lane;
           ewin = kb < kb_end ? __ldg(ue32 + size_t(nt * 4 + quarter) * kblocks + kb) : 0u;
         }
-        const uint32_t e4 = __shfl_sync(0xffffffffu, ewin, j & 31);
+        const uint32_t e4 = __shfl_sync(0xffffffffu, ewin, j - win);
 #pragma unroll
-        for (int g = 0; g < NG; ++g)
-          mul[g] = decode_multiplier_bf16x2(int((e4 >> (8 * (c_first / 2 + g))) & 0xFFu) - 127);
+        for (int q = 0; q < 4; ++q) mul[q] = decode_multiplier_bf16x2(int((e4 >> (8 * q)) & 0xFFu) - 127);
       } else {
 #pragma unroll
-        for (int g = 0; g < NG; ++g) mul[g] = decode_multiplier_bf16x2(0);
+        for (int q = 0; q < 4; ++q) mul[q] = decode_multiplier_bf16x2(0);
       }
       if (!warp_wait(&wfull[s], ph, abort_flag)) {
         raise_error(err, abort_flag, kSiteDecodeFull);
@@ -317,19 +332,21 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
       }
       // Chunk c of the 128-byte swizzled row sits at position c ^ (row & 7).
       const uint8_t* wrow = smem + size_t(s) * kStageW + row * 128;
-      uint4 raw[NC];
+      uint4 raw[8];
 #pragma unroll
-      for (int c = 0; c < NC; ++c)
-        raw[c] = *reinterpret_cast<const uint4*>(wrow + (((c + c_first) ^ (row & 7)) << 4));
+      for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(wrow + ((c ^ (row & 7)) << 4));
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty[s]);   // the codes are in registers: the stage can refill
-      if (++s == Q::kWStages) {
-        s = 0;
+      s += kIssuers;
+      if (s >= Q::kWStages) {
+        s -= Q::kWStages;
         ph ^= 1u;
       }
-      if (++j == nkb) {
-        j = 0;
+      j += kIssuers;
+      while (j >= nkb) {
+        j -= nkb;
         nt += num_clusters;
+        win = -32;
       }
       if (it >= kABufs) {
         const int prev = it - kABufs;   // K block whose MMA last read this A buffer
@@ -339,9 +356,9 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
         }
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_a + (uint32_t(quarter * 32) << 16) + uint32_t(a * kACols + c_first * 8);
+      const uint32_t taddr = tmem_a + (uint32_t(quarter * 32) << 16) + uint32_t(a * kACols);
 #pragma unroll
-      for (int h = 0; h < NG; ++h) {   // 32 codes -> 16 TMEM columns
+      for (int h = 0; h < 4; ++h) {   // 32 codes -> 16 TMEM columns
         uint32_t words[16];
         const uint32_t m = mul[h];
 #pragma unroll
@@ -364,6 +381,37 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
     griddep_wait();   // the output may still be read or written by the previous kernel
     const float* bs32 = static_cast<const float*>(scales);
     const int et = (warp - Q::kWarpEpi0) * 32 + lane;   // 0..127, work index in the cluster reduction
+    // Sums rows [rank * rows, (rank + 1) * rows) of tile q's partials over the
+    // cluster's ranks once all of them have published it, stores them, and
+    // hands the buffers back; false if a wait gave up.
+    auto reduce_tile = [&](int q) -> bool {
+      const int b = q & 1;
+      const float* rb = red + b * Q::kRedFloats;
+      if (!__all_sync(0xffffffffu, mbar_wait_acq_cluster(&red_full[b], uint32_t(q >> 1) & 1u, abort_flag))) {
+        raise_error(err, abort_flag, kSiteReduceFull);
+        return false;
+      }
+      const int rows = BN / split;
+      const int rl = et % rows;
+      const int n_out = (cluster_id + q * num_clusters) * BN + rank * rows + rl;
+      for (int m = et / rows; m < M; m += split) {
+        const uint32_t local = smem_u32(rb + m * BN + rank * rows + rl);
+        float v[kMaxSplitK];
+#pragma unroll
+        for (int r = 0; r < kMaxSplitK; ++r)
+          if (r < split) v[r] = ld_dsmem_f32(map_shared_rank(local, uint32_t(r)));
+        float sum = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxSplitK; ++r)
+          if (r < split) sum += v[r];
+        C[size_t(m) * ldc + n_out] = __float2bfloat16_rn(sum);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        for (int r = 0; r < split; ++r) mbar_arrive_cluster_relaxed(map_shared_rank(smem_u32(&red_empty[b]), r));
+      }
+      return true;
+    };
     bool ok = true;
     for (int q = 0; q < my_tiles && ok; ++q) {
       const int nt = cluster_id + q * num_clusters;
@@ -402,20 +450,20 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
         for (int c = 0; c < TM; ++c) acc[c] = fmaf(__uint_as_float(p[c]), sc, acc[c]);
       }
       if (!ok) break;
-      const int n = nt * BN + row;
       if (split == 1) {
+        const int n = nt * BN + row;
 #pragma unroll
         for (int m = 0; m < TM; ++m)
           if (m < M) C[size_t(m) * ldc + n] = __float2bfloat16_rn(acc[m]);
         continue;
       }
-      // ---- cluster reduction of this tile: every rank publishes its partial
-      // in its own shared memory, then sums one 128/split-row slice over all
-      // ranks in rank order and stores it.
+      // ---- cluster reduction: every rank publishes its partial of tile q in
+      // its own shared memory now, and sums one 128/split-row slice of tile
+      // q - 1 over all ranks (in rank order) afterwards, so a peer that runs
+      // behind does not hold up this rank's accumulation of the next tile.
       const int b = q & 1;
-      const uint32_t u = uint32_t(q >> 1);
       float* rb = red + b * Q::kRedFloats;   // [TM][BN]
-      if (q >= 2 && !warp_wait(&red_empty[b], (u & 1u) ^ 1u, abort_flag)) {
+      if (q >= 2 && !warp_wait(&red_empty[b], (uint32_t(q >> 1) & 1u) ^ 1u, abort_flag)) {
         raise_error(err, abort_flag, kSiteReduceEmpty);
         break;
       }
@@ -427,31 +475,12 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
         fence_acq_rel_cluster();   // this warp's partial is visible before the arrivals below
         for (int r = 0; r < split; ++r) mbar_arrive_cluster_relaxed(map_shared_rank(smem_u32(&red_full[b]), r));
       }
-      const bool got = __all_sync(0xffffffffu, mbar_wait_acq_cluster(&red_full[b], u & 1u, abort_flag));
-      if (!got) {
-        raise_error(err, abort_flag, kSiteReduceFull);
+      if (q >= 1 && !reduce_tile(q - 1)) {
+        ok = false;
         break;
       }
-      const int rows = BN / split;
-      const int rl = et % rows;
-      const int n_out = nt * BN + rank * rows + rl;
-      for (int m = et / rows; m < M; m += split) {
-        const uint32_t local = smem_u32(rb + m * BN + rank * rows + rl);
-        float v[kMaxSplitK];
-#pragma unroll
-        for (int r = 0; r < kMaxSplitK; ++r)
-          if (r < split) v[r] = ld_dsmem_f32(map_shared_rank(local, uint32_t(r)));
-        float sum = 0.f;
-#pragma unroll
-        for (int r = 0; r < kMaxSplitK; ++r)
-          if (r < split) sum += v[r];
-        C[size_t(m) * ldc + n_out] = __float2bfloat16_rn(sum);
-      }
-      __syncwarp();
-      if (lane == 0) {
-        for (int r = 0; r < split; ++r) mbar_arrive_cluster_relaxed(map_shared_rank(smem_u32(&red_empty[b]), r));
-      }
     }
+    if (ok && split > 1 && my_tiles > 0) reduce_tile(my_tiles - 1);
   }
 
   __syncwarp();   // single-lane roles rejoin their warp before the aligned barriers below
