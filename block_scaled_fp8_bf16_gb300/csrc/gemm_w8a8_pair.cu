@@ -17,13 +17,21 @@
 //   warps 0, 2   TMA producers for this CTA's A rows + scales (warp 0) and B
 //                rows (warp 2).
 //   warp 1       TMEM allocation (with the peer, 512 columns = two 256-column
-//                partials); in the even CTA one thread issues the MMAs and
-//                commits to both CTAs' barriers.  Both CTAs' operand copies
-//                complete on the even CTA's stage barrier (.cta_group::2
-//                TMA), so the MMA issuer waits on one barrier per stage.
+//                partials).
+//   warps 1, 3   in the even CTA, one thread each issues the MMAs of every
+//                other K block (the block's partial buffer is fixed by its
+//                parity) and commits to both CTAs' barriers.  A single thread
+//                needs longer to issue a K block's four pair MMAs than the
+//                tensor cores need to run them, so two issue in turn.  Both
+//                CTAs' operand copies complete on the even CTA's stage
+//                barrier (.cta_group::2 TMA), so an issuer waits on one
+//                barrier per stage.
 //   warps 4..11  promotion + epilogue, 8 warps: TMEM lane quarter = warp % 4,
-//                128 of the 256 columns each; acc = fma(partial, As*Bs, acc);
-//                bf16 store at the end of the tile.
+//                128 of the 256 columns each; acc = fma(partial, As*Bs, acc).
+//                At the end of a tile each warp writes its 32 x 128 bf16
+//                block to shared memory in the 128-byte swizzled layout and
+//                one lane stores it with two TMA tensor stores (coalesced,
+//                asynchronous; rows past M are clipped by the tensor map).
 // Tiles of the pair run persistently in grouped raster order ("Blockwise FP8
 // on Ada GPUs, part 2", "One tile doesn't fit all M": launch-order swizzle).
 #include <cuda_bf16.h>
@@ -38,13 +46,19 @@ constexpr int TM = 128;              // A rows per CTA (256 per pair)
 constexpr int PN = 256;              // C columns per pair tile (MMA N)
 constexpr int HN = PN / 2;           // B rows per CTA
 constexpr int BK = 128;              // one scale block of K
-constexpr int kStages = 6;
+// An even number of stages keeps every stage with one issuer (stage s holds
+// the K blocks of parity s & 1), so each issuer waits on every phase of its
+// stages in order and a parity wait can never mistake an old phase for a new one.
+constexpr int kStages = 4;
 constexpr int kStageA = TM * BK;
 constexpr int kStageB = HN * BK;
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kStageAs = TM * 4;
 constexpr int kAsStages = 16;        // scale ring, deeper than the operand ring so it never gates it
 constexpr int kEpiWarps = 8;
+constexpr int kIssuers = 2;                     // MMA-issuing threads (even CTA)
+constexpr int kStageC = 32 * 64 * 2;            // one 32-row x 64-column bf16 box, 128-byte swizzled
+constexpr int kBoxesPerWarp = 2;                // a warp's 32 x 128 output block
 constexpr int kThreads = 128 + kEpiWarps * 32;   // 384: three warpgroups
 constexpr int kCols = PN / (kEpiWarps / 4);      // 128 columns per epilogue thread
 constexpr int kChunk = 32;                       // columns per tcgen05.ld
@@ -57,7 +71,13 @@ constexpr uint32_t kTmemCols = kAccBufs * PN;
 constexpr uint32_t kIdesc = make_idesc(0 /* e4m3 */, 2 * TM, PN);
 constexpr int kGroupM = 8;
 constexpr int kBarrierBytes = 1024;
-constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + size_t(kAsStages) * kStageAs + kBarrierBytes + 1024;
+constexpr size_t kAsOff = size_t(kStages) * kStageBytes;
+constexpr size_t kCOff = kAsOff + size_t(kAsStages) * kStageAs;   // kEpiWarps staging boxes
+constexpr size_t kBarOff = kCOff + size_t(kEpiWarps) * kBoxesPerWarp * kStageC;
+constexpr size_t kSmemBytes = kBarOff + kBarrierBytes + 1024;
+static_assert(kCOff % 1024 == 0 && kStageC % 1024 == 0, "swizzled staging boxes need 1024-byte alignment");
+static_assert(kAccBufs == kIssuers, "each issuer owns one partial buffer");
+static_assert(kStages % kIssuers == 0, "each stage belongs to one issuer");
 
 static_assert(kTmemCols == 512, "two 256-column partials fill TMEM");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -103,28 +123,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   }
 }
 
-__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const float2* acc) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < kCols / 8; ++i) {
-    uint4 v;
-    v.x = pack_bf16x2(acc[4 * i + 0].x, acc[4 * i + 0].y);
-    v.y = pack_bf16x2(acc[4 * i + 1].x, acc[4 * i + 1].y);
-    v.z = pack_bf16x2(acc[4 * i + 2].x, acc[4 * i + 2].y);
-    v.w = pack_bf16x2(acc[4 * i + 3].x, acc[4 * i + 3].y);
-    d[i] = v;
-  }
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmAs, const float* __restrict__ Bs,
-                     __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N, int K, int* __restrict__ err) {
+                     const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmC,
+                     const float* __restrict__ Bs, int M, int N, int K, int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  float* as_stage = reinterpret_cast<float*>(smem + size_t(kStages) * kStageBytes);   // [kAsStages][TM]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes + size_t(kAsStages) * kStageAs);
+  float* as_stage = reinterpret_cast<float*>(smem + kAsOff);   // [kAsStages][TM]
+  uint8_t* c_stage = smem + kCOff;                              // [kEpiWarps][kBoxesPerWarp][kStageC]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* empty = full + kStages;
   uint64_t* as_full = empty + kStages;
   uint64_t* as_empty = as_full + kAsStages;
@@ -159,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&dfull[d], 1);
       mbar_init(&dempty[d], 2 * kEpiWarps);   // both CTAs' epilogues (used in the even CTA)
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, kIssuers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -171,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmAs);
+    tma_prefetch_desc(&tmC);
   }
   tc_fence_before();
   __syncthreads();
@@ -235,18 +244,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (uint32_t j = first_as; j < it; ++j) mbar_wait(&as_full[j % kAsStages], (j / kAsStages) & 1u, nullptr);
       }
     }
-  } else if (warp == 1) {
+  } else {
     if (lane == 0 && rank == 0) {
-      // ---------------------------------------------------------- MMA issuer (even CTA)
-      uint32_t it = 0, acc_it = 0;
+      // ---------------------------------------------------------- MMA issuers (even CTA, warps 1 and 3)
+      // Issuer w takes the K blocks with item parity w; they accumulate into
+      // partial buffer w, so the two issuers' MMAs never touch the same
+      // TMEM columns or operand stage.
+      const uint32_t w = warp == 1 ? 0u : 1u;
+      uint32_t it = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        for (int kb = 0; kb < kblocks; ++kb, ++it, ++acc_it) {
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          if ((it & 1u) != w) continue;
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          const int d = acc_it % kAccBufs;
-          const uint32_t dph = (acc_it / kAccBufs) & 1u;
-          if (!mbar_wait_cluster(&dempty[d], dph ^ 1u, abort_flag)) {
+          const uint32_t dph = (it / kAccBufs) & 1u;
+          if (!mbar_wait_cluster(&dempty[w], dph ^ 1u, abort_flag)) {
             raise_error(err, abort_flag, kSiteMmaAccEmpty);
             ok = false;
             break;
@@ -259,14 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + size_t(s) * kStageBytes);
           const uint32_t b0 = a0 + kStageA;
-          const uint32_t d_tmem = tmem + uint32_t(d * PN);
+          const uint32_t d_tmem = tmem + w * uint32_t(PN);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
             mma_f8_ss_pair(d_tmem, desc_sw128_kmajor(a0 + 32u * k), desc_sw128_kmajor(b0 + 32u * k), kIdesc,
                            k > 0 ? 1u : 0u);
           }
           mma_commit_pair_mc(&empty[s], 0x3);
-          mma_commit_pair_mc(&dfull[d], 0x3);
+          mma_commit_pair_mc(&dfull[w], 0x3);
         }
       }
       mma_commit_pair_mc(drain, 0x1);
@@ -281,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = (e >> 2) * kCols;
     const int row = quarter * 32 + lane;
     const uint32_t dempty0 = map_shared_rank(smem_u32(dempty), 0);
+    uint8_t* stg = c_stage + size_t(e) * kBoxesPerWarp * kStageC;
     griddep_wait();   // the output may still be read or written by the previous kernel
     float2 acc[kCols / 2];
     uint32_t it = 0;
@@ -288,9 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = pair; t < num_tiles && ok; t += num_pairs) {
       int mt, nt;
       tile_coords(t, m_tiles, n_tiles, mt, nt);
-      const int m = mt * 2 * TM + rank * TM + row;
+      const int y = mt * 2 * TM + rank * TM + quarter * 32;   // first row of this warp's 32-row block
       const int n = nt * PN + col0;
-      const bool row_ok = m < M;
       const bool col_ok = n < N;
 #pragma unroll
       for (int j = 0; j < kCols / 2; ++j) acc[j] = make_float2(0.f, 0.f);
@@ -340,8 +353,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (ok && row_ok && col_ok) store_row(C + size_t(m) * ldc + n, acc);
+      if (ok && y < M && col_ok) {
+        // Two 32 x 64 boxes; chunk c (8 columns) of row r sits at 16-byte
+        // position c ^ (r & 7) of the row's 128 bytes (128-byte swizzle).
+        if (lane == 0) bulk_wait_group_read0();   // the previous tile's stores have left the staging buffers
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < kBoxesPerWarp; ++h) {
+          uint8_t* dst = stg + h * kStageC + lane * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float2* a = acc + h * 32 + 4 * c;
+            uint4 v;
+            v.x = pack_bf16x2(a[0].x, a[0].y);
+            v.y = pack_bf16x2(a[1].x, a[1].y);
+            v.z = pack_bf16x2(a[2].x, a[2].y);
+            v.w = pack_bf16x2(a[3].x, a[3].y);
+            *reinterpret_cast<uint4*>(dst + ((c ^ (lane & 7)) << 4)) = v;
+          }
+        }
+        fence_async_shared();   // generic-proxy writes become visible to the TMA engine
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < kBoxesPerWarp; ++h) tma_store_2d(&tmC, stg + h * kStageC, n + h * 64, y);
+          bulk_commit_group();
+        }
+      }
     }
+    if (lane == 0) bulk_wait_group0();   // the staging buffer stays valid until the stores are done
   }
 
   __syncwarp();
@@ -393,8 +433,7 @@ cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel, p.tmA, p.tmB, p.tmAs, p.Bs, static_cast<__nv_bfloat16*>(p.C),
-                            p.ldc, p.M, p.N, p.K, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel, p.tmA, p.tmB, p.tmAs, p.tmC, p.Bs, p.M, p.N, p.K, p.err);
 }
 
 }  // namespace fp8blk
