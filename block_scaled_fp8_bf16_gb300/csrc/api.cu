@@ -258,6 +258,9 @@ fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda, const float* a_s
   st = make_map(p.tmAs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scales, uint64_t(lds), uint64_t(K / 128),
                 uint64_t(lds) * 4, kW8A8TileM, 1, false);
   if (st != FP8BLK_OK) return st;
+  st = make_map(p.tmAsG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scales, uint64_t(lds), uint64_t(K / 128),
+                uint64_t(lds) * 4, kW8A8TileM, 8, false);
+  if (st != FP8BLK_OK) return st;
   st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c_bf16, uint64_t(N), uint64_t(M), uint64_t(ldc) * 2, 64, 32);
   if (st != FP8BLK_OK) return st;
   p.Bs = b_scales;

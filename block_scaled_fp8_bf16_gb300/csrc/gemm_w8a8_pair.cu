@@ -14,8 +14,8 @@
 // Roles per CTA (three warpgroups; registers are rebalanced with setmaxnreg
 // from 168 per thread at launch to 40 for warpgroup 0 and 232 for the two
 // epilogue warpgroups: 40*128 + 232*256 = 168*384, which the build checks):
-//   warps 0, 2   TMA producers for this CTA's A rows + scales (warp 0) and B
-//                rows (warp 2).
+//   warps 0, 2   TMA producers: this CTA's A rows + activation scales (warp 0,
+//                the scales eight K blocks per copy) and B rows (warp 2).
 //   warp 1       TMEM allocation (with the peer, 512 columns = two 256-column
 //                partials).
 //   warps 1, 3   in the even CTA, one thread each issues the MMAs of every
@@ -53,8 +53,9 @@ constexpr int kStages = 4;
 constexpr int kStageA = TM * BK;
 constexpr int kStageB = HN * BK;
 constexpr int kStageBytes = kStageA + kStageB;
-constexpr int kStageAs = TM * 4;
-constexpr int kAsStages = 16;        // scale ring, deeper than the operand ring so it never gates it
+constexpr int kAsGroup = 8;          // K blocks of activation scales per scale stage
+constexpr int kStageAs = kAsGroup * TM * 4;   // [kAsGroup][TM] fp32
+constexpr int kAsStages = 4;         // 32 K blocks of scales in flight: the ring never gates the operands
 constexpr int kEpiWarps = 8;
 constexpr int kIssuers = 2;                     // MMA-issuing threads (even CTA)
 constexpr int kStageC = 32 * 64 * 2;            // one 32-row x 64-column bf16 box, 128-byte swizzled
@@ -125,12 +126,12 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmC,
+                     const __grid_constant__ CUtensorMap tmAsG, const __grid_constant__ CUtensorMap tmC,
                      const float* __restrict__ Bs, int M, int N, int K, int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  float* as_stage = reinterpret_cast<float*>(smem + kAsOff);   // [kAsStages][TM]
+  float* as_stage = reinterpret_cast<float*>(smem + kAsOff);   // [kAsStages][kAsGroup][TM]
   uint8_t* c_stage = smem + kCOff;                              // [kEpiWarps][kBoxesPerWarp][kStageC]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* empty = full + kStages;
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmAs);
+    tma_prefetch_desc(&tmAsG);
     tma_prefetch_desc(&tmC);
   }
   tc_fence_before();
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Under programmatic dependent launch the weights stream in at once;
       // the activations and their scales wait for the previous kernel.
       if (a_side) griddep_wait();
-      uint32_t it = 0;
+      uint32_t it = 0, gi = 0;   // operand items and scale groups issued
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
         int mt, nt;
@@ -208,10 +209,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          const int j = it % kAsStages;
-          const uint32_t jph = (it / kAsStages) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag) ||
-              (a_side && !mbar_wait(&as_empty[j], jph ^ 1u, abort_flag))) {
+          if (a_side && kb % kAsGroup == 0) {
+            // Scales of K blocks kb .. kb + kAsGroup - 1 in one box (rows
+            // past K / 128 arrive zero-filled and are never read).
+            const int j = gi % kAsStages;
+            if (!mbar_wait(&as_empty[j], ((gi / kAsStages) & 1u) ^ 1u, abort_flag)) {
+              raise_error(err, abort_flag, kSiteProducerEmpty);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&as_full[j], kStageAs);
+            tma_load_2d(as_stage + j * (kAsGroup * TM), &tmAsG, &as_full[j], m0, kb);
+            ++gi;
+          }
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
             raise_error(err, abort_flag, kSiteProducerEmpty);
             ok = false;
             break;
@@ -222,8 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // only deliver them.
           const uint32_t full0 = full0_base + uint32_t(s) * 8u;
           if (a_side) {
-            mbar_arrive_expect_tx(&as_full[j], kStageAs);
-            tma_load_2d(as_stage + j * TM, &tmAs, &as_full[j], m0, kb);
             if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kStageA);
             tma_load_2d_pair(sa, &tmA, full0, kb * BK, m0);
           } else {
@@ -239,9 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0u;
         if (rank == 0)
           for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1u, nullptr);
-        const uint32_t first_as = it > uint32_t(kAsStages) ? it - kAsStages : 0u;
+        const uint32_t first_as = gi > uint32_t(kAsStages) ? gi - kAsStages : 0u;
         if (a_side)
-          for (uint32_t j = first_as; j < it; ++j) mbar_wait(&as_full[j % kAsStages], (j / kAsStages) & 1u, nullptr);
+          for (uint32_t j = first_as; j < gi; ++j) mbar_wait(&as_full[j % kAsStages], (j / kAsStages) & 1u, nullptr);
       }
     }
   } else {
@@ -297,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stg = c_stage + size_t(e) * kBoxesPerWarp * kStageC;
     griddep_wait();   // the output may still be read or written by the previous kernel
     float2 acc[kCols / 2];
-    uint32_t it = 0;
+    uint32_t it = 0, gi = 0;   // K blocks and scale groups consumed
     bool ok = true;
     for (int t = pair; t < num_tiles && ok; t += num_pairs) {
       int mt, nt;
@@ -312,18 +321,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         if ((kb & 31) == 0) bs_win = (col_ok && kb + lane < kblocks) ? __ldg(bs_row + kb + lane) : 0.f;
         const float sb = __shfl_sync(0xffffffffu, bs_win, kb & 31);
-        const int j = it % kAsStages;
-        const uint32_t jph = (it / kAsStages) & 1u;
+        const int j = gi % kAsStages;
         const int d = it % kAccBufs;
         const uint32_t dph = (it / kAccBufs) & 1u;
-        if (!__all_sync(0xffffffffu, mbar_wait(&as_full[j], jph, abort_flag))) {
+        if (kb % kAsGroup == 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&as_full[j], (gi / kAsStages) & 1u, abort_flag))) {
           raise_error(err, abort_flag, kSiteEpilogueFull);
           ok = false;
           break;
         }
-        const float sa = as_stage[j * TM + row];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&as_empty[j]);
+        const float sa = as_stage[(j * kAsGroup + kb % kAsGroup) * TM + row];
+        if (kb % kAsGroup == kAsGroup - 1 || kb == kblocks - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&as_empty[j]);
+          ++gi;
+        }
         if (!__all_sync(0xffffffffu, mbar_wait(&dfull[d], dph, abort_flag))) {
           raise_error(err, abort_flag, kSiteEpilogueFull);
           ok = false;
@@ -433,7 +445,7 @@ cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel, p.tmA, p.tmB, p.tmAs, p.tmC, p.Bs, p.M, p.N, p.K, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel, p.tmA, p.tmB, p.tmAsG, p.tmC, p.Bs, p.M, p.N, p.K, p.err);
 }
 
 }  // namespace fp8blk

@@ -74,6 +74,7 @@ struct GemmW8A8Args {
   CUtensorMap tmA;    // e4m3 [M, K], box {128 (K), 128 (M)}, 128B swizzle
   CUtensorMap tmB;    // e4m3 [N, K], box {128 (K), kW8A8TileN (N)}, 128B swizzle
   CUtensorMap tmAs;   // fp32 [K/128][lds] read as {M, K/128}, box {128, 1}, no swizzle
+  CUtensorMap tmAsG;  // the same scales, box {128, 8}: eight K blocks per copy (pair kernel)
   CUtensorMap tmC;    // bf16 [M, N] pitch ldc, box {64 (N), 32 (M)}, 128B swizzle (pair kernel's stores)
   const float* Bs;    // [N/128][K/128]
   void* C;            // bf16 [M, ldc]
