@@ -61,11 +61,10 @@ constexpr int kEpiWarps = 4;
 constexpr int kWarpXProducer = 1;
 constexpr int kWarpIssuer0 = 2;
 constexpr int kWarpDec0 = kWarpIssuer0 + kIssuers;
-constexpr int kXStages = 4;       // token tiles in flight
 constexpr int kABufs = 4;         // decoded A blocks in TMEM
 constexpr int kDBufs = 8;         // FP32 partials in TMEM
-constexpr int kRing = 8;          // MMA-completion barriers, indexed by K-block count
-constexpr int kBarrierBytes = 512;
+constexpr int kRing = 16;         // MMA-completion barriers, indexed by K-block count
+constexpr int kBarrierBytes = 1024;
 constexpr int kEarlyW = 4;        // weight stages requested before the setup barrier
 
 template <int TM>
@@ -77,7 +76,13 @@ struct DecCfg {
   static constexpr int kWarpEpi0 = kWarpDec0 + kDecWarps;
   static constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
   static constexpr int kStageX = TM * BK * 2;
-  static constexpr int kWStages = TM == 16 ? 12 : 10;          // weight ring, as deep as shared memory allows
+  // Token tiles are refilled only after the MMA that read them has
+  // completed, and while the weights stream at full rate an L2 refill takes
+  // a few thousand cycles, so the token ring is deep (16 or 8 tiles = 64 KB).
+  // Eight weight stages (128 KB per SM, ~19 MB over the GPU) already keep
+  // HBM saturated.
+  static constexpr int kXStages = TM == 16 ? 16 : 8;
+  static constexpr int kWStages = 8;
   static constexpr int kRedFloats = BN * TM;                   // one partial tile, token-major [TM][BN]
   static constexpr size_t kXOff = size_t(kWStages) * kStageW;
   static constexpr size_t kRedOff = kXOff + size_t(kXStages) * kStageX;
@@ -128,7 +133,7 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + Q::kBarOff);
   uint64_t* wempty = wfull + Q::kWStages;
   uint64_t* xfull = wempty + Q::kWStages;
-  uint64_t* afull = xfull + kXStages;
+  uint64_t* afull = xfull + Q::kXStages;
   uint64_t* mdone = afull + kABufs;
   uint64_t* dempty = mdone + kRing;
   uint64_t* red_full = dempty + kDBufs;
@@ -167,7 +172,7 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], 4);   // the four warps of one decode group
     }
-    for (int j = 0; j < kXStages; ++j) mbar_init(&xfull[j], 1);
+    for (int j = 0; j < Q::kXStages; ++j) mbar_init(&xfull[j], 1);
     for (int i = 0; i < kABufs; ++i) mbar_init(&afull[i], 4);
     for (int i = 0; i < kRing; ++i) mbar_init(&mdone[i], 1);
     for (int i = 0; i < kDBufs; ++i) mbar_init(&dempty[i], kEpiWarps);
@@ -246,8 +251,8 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
       griddep_wait();   // activations may come from the previous kernel
       int it = 0;
       for (; it < n_items; ++it) {
-        const int j = it % kXStages;
-        const int prev = it - kXStages;   // K block whose MMA last read this slot
+        const int j = it % Q::kXStages;
+        const int prev = it - Q::kXStages;   // K block whose MMA last read this slot
         if (prev >= 0 && !mbar_wait_sleep(&mdone[prev % kRing], uint32_t(prev / kRing) & 1u, abort_flag)) {
           raise_error(err, abort_flag, kSiteProducerEmpty);
           break;
@@ -259,8 +264,8 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
         tma_load_2d(sx + TM * 128, &tmX, &xfull[j], kb * BK + 64, 0);
       }
       if (it < n_items) {
-        const int first = it > kXStages ? it - kXStages : 0;
-        for (int j = first; j < it; ++j) mbar_wait(&xfull[j % kXStages], uint32_t(j / kXStages) & 1u, nullptr);
+        const int first = it > Q::kXStages ? it - Q::kXStages : 0;
+        for (int j = first; j < it; ++j) mbar_wait(&xfull[j % Q::kXStages], uint32_t(j / Q::kXStages) & 1u, nullptr);
       }
     }
   } else if (warp < kWarpDec0) {
@@ -270,13 +275,13 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
       for (int it = w; it < n_items; it += kIssuers) {
         const int d = it % kDBufs;
         const int a = it % kABufs;
-        const int j = it % kXStages;
+        const int j = it % Q::kXStages;
         if (it >= kDBufs && !mbar_wait_sleep(&dempty[d], (uint32_t(it / kDBufs) & 1u) ^ 1u, abort_flag)) {
           raise_error(err, abort_flag, kSiteMmaAccEmpty);
           break;
         }
         if (!mbar_wait_sleep(&afull[a], uint32_t(it / kABufs) & 1u, abort_flag) ||
-            !mbar_wait_sleep(&xfull[j], uint32_t(it / kXStages) & 1u, abort_flag)) {
+            !mbar_wait_sleep(&xfull[j], uint32_t(it / Q::kXStages) & 1u, abort_flag)) {
           raise_error(err, abort_flag, kSiteMmaAFull);
           break;
         }
