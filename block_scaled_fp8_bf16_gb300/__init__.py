@@ -49,6 +49,7 @@ EXPORTS = {
     "fp8blk_quant_weight": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "fp8blk_validate_weights": (_I32, [_P, _I64, _P, _I32, _I64, _I64, _P, _P]),
     "fp8blk_debug_decode_e4m3": (_I32, [_P, _I64, _I32, _P, _P]),
+    "fp8blk_debug_wait_timeout": (_I32, [_I64, _P]),
     "fp8blk_query_constraints": (_I32, [_P]),
     "fp8blk_status_string": (ctypes.c_char_p, [_I32]),
     "fp8blk_device_error": (_I32, [_P, _I32]),
@@ -188,6 +189,16 @@ def fp8blk_validate_weights(b, b_scales, fmt, dev_counts, stream=None):
 def fp8blk_debug_decode_e4m3(codes, exp_shift, out, stream=None):
     _check(_L().fp8blk_debug_decode_e4m3(_ptr(codes), codes.numel(), int(exp_shift), _ptr(out), _stream(stream)),
            "fp8blk_debug_decode_e4m3")
+
+
+DIAG_TIMEOUT_CODE = 0x4F01   # FP8BLK_DIAG_TIMEOUT_CODE in the header
+
+
+def fp8blk_debug_wait_timeout(limit_ns: int, stream=None):
+    """Launches the bounded-wait failure check: one warp waits limit_ns on an
+    mbarrier nobody completes, then records DIAG_TIMEOUT_CODE in the device
+    error word and returns."""
+    _check(_L().fp8blk_debug_wait_timeout(int(limit_ns), _stream(stream)), "fp8blk_debug_wait_timeout")
 
 
 def fp8blk_query_constraints() -> dict:

@@ -344,6 +344,15 @@ fp8blk_status fp8blk_debug_decode_e4m3(const void* codes, int64_t n, int32_t exp
   return cuda_status(launch_debug_decode(codes, n, exp_shift, out_bf16, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8blk_status fp8blk_debug_wait_timeout(int64_t limit_ns, fp8blk_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 100000000) return FP8BLK_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  fp8blk_status st = device_info(dev);
+  if (st != FP8BLK_OK) return st;
+  return cuda_status(launch_debug_wait_timeout(limit_ns, FP8BLK_DIAG_TIMEOUT_CODE, dev.err_word,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 fp8blk_status fp8blk_query_constraints(fp8blk_constraints* out) {
   if (!out) return FP8BLK_ERR_INVALID_ARG;
   out->abi_version = FP8BLK_ABI_VERSION;

@@ -68,6 +68,7 @@ struct ValidateArgs {
 cudaError_t launch_validate(const ValidateArgs& p, const DeviceInfo& dev, cudaStream_t s);
 
 cudaError_t launch_debug_decode(const void* codes, int64_t n, int exp_shift, void* out, cudaStream_t s);
+cudaError_t launch_debug_wait_timeout(int64_t limit_ns, int code, int* err, cudaStream_t s);
 
 // ------------------------------------------------------------------ W8A8
 struct GemmW8A8Args {

@@ -1,5 +1,5 @@
 // Quantisers (bf16 -> e4m3 with fp32 block scales), the weight validator and
-// the decode diagnostic.
+// the decode and wait-timeout diagnostics.
 //
 // Per-token activation quantisation ("Blockwise FP8 on Ada GPUs, part 2",
 // "The starting point": one scale per token per 128 values of K) follows the
@@ -273,6 +273,27 @@ cudaError_t launch_validate(const ValidateArgs& p, const DeviceInfo& dev, cudaSt
   const int grid = grid_for(p.N * (p.K / 16), 256, dev.num_sms, 8);
   validate_kernel<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(p.b), p.ldb, p.scales, p.fmt, p.N, p.K,
                                        p.counts);
+  return cudaGetLastError();
+}
+
+// Waits on an mbarrier that no thread ever arrives on, with the bounded-wait
+// loop of the GEMM kernels (try_wait polling, %globaltimer limit), and
+// records `code` in the error word when the limit passes.
+__global__ void debug_wait_timeout_kernel(int64_t limit_ns, int code, int* __restrict__ err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  bool done = mbar_test(&bar, 0);
+  const uint64_t t0 = globaltimer_ns();
+  while (!done && globaltimer_ns() - t0 < uint64_t(limit_ns)) done = mbar_test(&bar, 0);
+  if (!done && threadIdx.x == 0) atomicCAS(err, 0, code);
+}
+
+cudaError_t launch_debug_wait_timeout(int64_t limit_ns, int code, int* err, cudaStream_t s) {
+  debug_wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, code, err);
   return cudaGetLastError();
 }
 

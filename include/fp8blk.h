@@ -244,6 +244,21 @@ FP8BLK_API fp8blk_status fp8blk_validate_weights(const void* b_e4m3, int64_t ldb
 FP8BLK_API fp8blk_status fp8blk_debug_decode_e4m3(const void* codes, int64_t n, int32_t exp_shift,
                                        void* out_bf16, fp8blk_stream_t stream);
 
+/*
+ * Failure-detection check of the bounded waits (no counterpart in the pages;
+ * it exercises the library's own error path).  Launches one warp that
+ * initialises an mbarrier nobody arrives on and waits for it with the same
+ * bounded-wait loop the GEMM kernels use, but with a limit of limit_ns
+ * nanoseconds of %globaltimer instead of one second.  When the limit passes
+ * the kernel writes FP8BLK_DIAG_TIMEOUT_CODE into the device error word (if
+ * it is still 0) and returns normally, so the CUDA context stays usable; the
+ * caller then sees FP8BLK_ERR_TIMEOUT from fp8blk_device_error().
+ * limit_ns must lie in [1000, 100000000] (1 us .. 100 ms), else
+ * FP8BLK_ERR_INVALID_ARG before any device work.  Asynchronous on stream.
+ */
+#define FP8BLK_DIAG_TIMEOUT_CODE 0x4F01
+FP8BLK_API fp8blk_status fp8blk_debug_wait_timeout(int64_t limit_ns, fp8blk_stream_t stream);
+
 /* Fills *out with the kernels' compile-time constraints.  No device needed. */
 FP8BLK_API fp8blk_status fp8blk_query_constraints(fp8blk_constraints* out);
 

@@ -160,3 +160,9 @@ def test_valid_call_without_gpu_reports_cuda_or_arch(fp8blk):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert call_w8a8(fp8blk._L()) in (4, 5)
+
+
+def test_wait_timeout_diag_argument_errors(fp8blk):
+    L = fp8blk._L()
+    for bad in (0, 999, 100_000_001, -5):
+        assert L.fp8blk_debug_wait_timeout(bad, None) == 1   # FP8BLK_ERR_INVALID_ARG, no device work
