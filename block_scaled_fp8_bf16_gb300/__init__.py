@@ -23,6 +23,7 @@ SCALE_UE8M0_32x32 = 1
 
 # Launch flags of the GEMM entry points (FP8BLK_FLAG_* in the header).
 FLAG_PDL = 1
+FLAG_OUT_F32 = 2
 
 STATUS_NAMES = {
     0: "FP8BLK_OK",
@@ -127,6 +128,13 @@ def _bytes_tensor(t):
     return t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t
 
 
+def _out_flags(c, flags):
+    """The GEMM output is bf16 or float32; a float32 tensor selects FLAG_OUT_F32."""
+    import torch
+    _expect(c, (torch.bfloat16, torch.float32), "c")
+    return int(flags) | (FLAG_OUT_F32 if c.dtype == torch.float32 else 0)
+
+
 def _expect(t, dtypes, name):
     if t.dtype not in dtypes:
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
@@ -145,12 +153,12 @@ def fp8blk_quant_act(x, a, a_scales, stream=None):
 
 
 def fp8blk_gemm_w8a8(a, a_scales, b, b_scales, c, stream=None, flags=0):
-    """C[M, N] bf16 = block-scaled a[M, K] e4m3 x b[N, K] e4m3."""
+    """C[M, N] (bf16, or float32 when c is float32) = block-scaled a[M, K] e4m3 x b[N, K] e4m3."""
     a, b = _bytes_tensor(a), _bytes_tensor(b)
     M, K = a.shape
     N = b.shape[0]
     _check(_L().fp8blk_gemm_w8a8(_ptr(a), _ld(a), _ptr(a_scales), _ld(a_scales), _ptr(b), _ld(b), _ptr(b_scales),
-                                _ptr(c), _ld(c), M, N, K, int(flags), _stream(stream)), "fp8blk_gemm_w8a8")
+                                _ptr(c), _ld(c), M, N, K, _out_flags(c, flags), _stream(stream)), "fp8blk_gemm_w8a8")
 
 
 def fp8blk_gemm_w8a16(x, b, b_scales, fmt, c, stream=None, flags=0):
@@ -159,7 +167,7 @@ def fp8blk_gemm_w8a16(x, b, b_scales, fmt, c, stream=None, flags=0):
     M, K = x.shape
     N = b.shape[0]
     _check(_L().fp8blk_gemm_w8a16(_ptr(x), _ld(x), _ptr(b), _ld(b), _ptr(b_scales), int(fmt), _ptr(c), _ld(c),
-                                 M, N, K, int(flags), _stream(stream)), "fp8blk_gemm_w8a16")
+                                 M, N, K, _out_flags(c, flags), _stream(stream)), "fp8blk_gemm_w8a16")
 
 
 def fp8blk_gemv_w8a16(x, b, b_scales, fmt, c, stream=None, flags=0):
@@ -168,7 +176,7 @@ def fp8blk_gemv_w8a16(x, b, b_scales, fmt, c, stream=None, flags=0):
     M, K = x.shape
     N = b.shape[0]
     _check(_L().fp8blk_gemv_w8a16(_ptr(x), _ld(x), _ptr(b), _ld(b), _ptr(b_scales), int(fmt), _ptr(c), _ld(c),
-                                 M, N, K, int(flags), _stream(stream)), "fp8blk_gemv_w8a16")
+                                 M, N, K, _out_flags(c, flags), _stream(stream)), "fp8blk_gemv_w8a16")
 
 
 def fp8blk_quant_weight(w, b, b_scales, stream=None):
@@ -240,26 +248,26 @@ def quant_weight(w, stream=None):
     return b, s
 
 
-def gemm_w8a8(a, a_scales, b, b_scales, out=None, stream=None, flags=0):
+def gemm_w8a8(a, a_scales, b, b_scales, out=None, stream=None, flags=0, out_dtype=None):
     import torch
     if out is None:
-        out = torch.empty((a.shape[0], b.shape[0]), dtype=torch.bfloat16, device=a.device)
+        out = torch.empty((a.shape[0], b.shape[0]), dtype=out_dtype or torch.bfloat16, device=a.device)
     fp8blk_gemm_w8a8(a, a_scales, b, b_scales, out, stream, flags)
     return out
 
 
-def gemm_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None, flags=0):
+def gemm_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None, flags=0, out_dtype=None):
     import torch
     if out is None:
-        out = torch.empty((x.shape[0], b.shape[0]), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((x.shape[0], b.shape[0]), dtype=out_dtype or torch.bfloat16, device=x.device)
     fp8blk_gemm_w8a16(x, b, b_scales, fmt, out, stream, flags)
     return out
 
 
-def gemv_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None, flags=0):
+def gemv_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None, flags=0, out_dtype=None):
     import torch
     if out is None:
-        out = torch.empty((x.shape[0], b.shape[0]), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((x.shape[0], b.shape[0]), dtype=out_dtype or torch.bfloat16, device=x.device)
     fp8blk_gemv_w8a16(x, b, b_scales, fmt, out, stream, flags)
     return out
 

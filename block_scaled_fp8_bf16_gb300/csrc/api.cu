@@ -150,14 +150,14 @@ fp8blk_status make_map(CUtensorMap& out, CUtensorMapDataType dtype, const void* 
 
 // ------------------------------------------------------------------ checks
 
-constexpr uint32_t kKnownFlags = FP8BLK_FLAG_PDL;
+constexpr uint32_t kKnownFlags = FP8BLK_FLAG_PDL | FP8BLK_FLAG_OUT_F32;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline fp8blk_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8BLK_OK : FP8BLK_ERR_CUDA; }
 
 fp8blk_status check_w8a16_args(const void* x, int64_t ldx, const void* b, int64_t ldb, const void* sc, int fmt,
-                               const void* c, int64_t ldc, int64_t M, int64_t N, int64_t K) {
+                               const void* c, int64_t ldc, int64_t M, int64_t N, int64_t K, int64_t c_elem) {
   if (M < 0 || N < 0 || K < 0) return FP8BLK_ERR_INVALID_ARG;
   if (fmt != FP8BLK_SCALE_F32_128x128 && fmt != FP8BLK_SCALE_UE8M0_32x32) return FP8BLK_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
@@ -169,12 +169,12 @@ fp8blk_status check_w8a16_args(const void* x, int64_t ldx, const void* b, int64_
   if (ldx < K || ldb < K || ldc < N) return FP8BLK_ERR_INVALID_ARG;
   if ((x && !aligned16(x)) || (b && !aligned16(b)) || (sc && !aligned16(sc)) || !aligned16(c))
     return FP8BLK_ERR_MISALIGNED;
-  if ((ldx * 2) % 16 != 0 || ldb % 16 != 0 || (ldc * 2) % 16 != 0) return FP8BLK_ERR_MISALIGNED;
+  if ((ldx * 2) % 16 != 0 || ldb % 16 != 0 || (ldc * c_elem) % 16 != 0) return FP8BLK_ERR_MISALIGNED;
   return FP8BLK_OK;
 }
 
-fp8blk_status zero_output(void* c, int64_t ldc, int64_t M, int64_t N, cudaStream_t s) {
-  return cuda_status(cudaMemset2DAsync(c, size_t(ldc) * 2, 0, size_t(N) * 2, size_t(M), s));
+fp8blk_status zero_output(void* c, int64_t ldc, int64_t M, int64_t N, int64_t elem, cudaStream_t s) {
+  return cuda_status(cudaMemset2DAsync(c, size_t(ldc * elem), 0, size_t(N * elem), size_t(M), s));
 }
 
 fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, const void* sc, int fmt, void* c,
@@ -182,7 +182,8 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   DeviceInfo dev;
   fp8blk_status st = device_info(dev);
   if (st != FP8BLK_OK) return st;
-  if (K == 0) return zero_output(c, ldc, M, N, s);
+  const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
+  if (K == 0) return zero_output(c, ldc, M, N, f32 ? 4 : 2, s);
   const bool decode = M <= kW8A16DecodeMaxM;
   const int tile_m = decode ? (M <= 16 ? 16 : 32) : w8a16_pick_tile_m(M);
   GemmW8A16Args p;
@@ -200,6 +201,7 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   p.K = int(K);
   p.tile_m = tile_m;
   p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
+  p.out_f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
   p.err = dev.err_word;
   return cuda_status(decode ? launch_w8a16_decode(p, dev, s) : launch_gemm_w8a16(p, dev, s));
 }
@@ -240,12 +242,14 @@ fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda, const float* a_s
   if ((a_e4m3 && !aligned16(a_e4m3)) || (a_scales && !aligned16(a_scales)) || (b_e4m3 && !aligned16(b_e4m3)) ||
       (b_scales && !aligned16(b_scales)) || !aligned16(c_bf16))
     return FP8BLK_ERR_MISALIGNED;
-  if (lda % 16 != 0 || ldb % 16 != 0 || (ldc * 2) % 16 != 0 || lds % 4 != 0) return FP8BLK_ERR_MISALIGNED;
+  const int64_t c_elem = (flags & FP8BLK_FLAG_OUT_F32) ? 4 : 2;
+  if (lda % 16 != 0 || ldb % 16 != 0 || (ldc * c_elem) % 16 != 0 || lds % 4 != 0) return FP8BLK_ERR_MISALIGNED;
   DeviceInfo dev;
   fp8blk_status st = device_info(dev);
   if (st != FP8BLK_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (K == 0) return zero_output(c_bf16, ldc, M, N, s);
+  const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
+  if (K == 0) return zero_output(c_bf16, ldc, M, N, f32 ? 4 : 2, s);
   GemmW8A8Args p;
   st = make_map(p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_e4m3, uint64_t(K), uint64_t(M), uint64_t(lda), 128,
                 kW8A8TileM);
@@ -261,7 +265,11 @@ fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda, const float* a_s
   st = make_map(p.tmAsG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scales, uint64_t(lds), uint64_t(K / 128),
                 uint64_t(lds) * 4, kW8A8TileM, 8, false);
   if (st != FP8BLK_OK) return st;
-  st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c_bf16, uint64_t(N), uint64_t(M), uint64_t(ldc) * 2, 64, 32);
+  // Output boxes of 32 rows x 128 bytes (64 bf16 or 32 float32 columns).
+  if (f32)
+    st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c_bf16, uint64_t(N), uint64_t(M), uint64_t(ldc) * 4, 32, 32);
+  else
+    st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c_bf16, uint64_t(N), uint64_t(M), uint64_t(ldc) * 2, 64, 32);
   if (st != FP8BLK_OK) return st;
   p.Bs = b_scales;
   p.C = c_bf16;
@@ -270,6 +278,7 @@ fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda, const float* a_s
   p.N = int(N);
   p.K = int(K);
   p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
+  p.out_f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
   p.err = dev.err_word;
   return cuda_status(launch_gemm_w8a8(p, dev, s));
 }
@@ -278,7 +287,8 @@ fp8blk_status fp8blk_gemm_w8a16(const void* x_bf16, int64_t ldx, const void* b_e
                                 const void* b_scales, fp8blk_scale_fmt fmt, void* c_bf16, int64_t ldc, int64_t M,
                                 int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
   if ((flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
-  fp8blk_status st = check_w8a16_args(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K);
+  fp8blk_status st = check_w8a16_args(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K,
+                                      (flags & FP8BLK_FLAG_OUT_F32) ? 4 : 2);
   if (st != FP8BLK_OK || M == 0 || N == 0) return st;
   return run_w8a16(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K, flags,
                    reinterpret_cast<cudaStream_t>(stream));
@@ -288,7 +298,8 @@ fp8blk_status fp8blk_gemv_w8a16(const void* x_bf16, int64_t ldx, const void* b_e
                                 const void* b_scales, fp8blk_scale_fmt fmt, void* c_bf16, int64_t ldc, int64_t M,
                                 int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
   if ((flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
-  fp8blk_status st = check_w8a16_args(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K);
+  fp8blk_status st = check_w8a16_args(x_bf16, ldx, b_e4m3, ldb, b_scales, int(fmt), c_bf16, ldc, M, N, K,
+                                      (flags & FP8BLK_FLAG_OUT_F32) ? 4 : 2);
   if (st != FP8BLK_OK) return st;
   if (M > 16) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
   if (M == 0 || N == 0) return FP8BLK_OK;

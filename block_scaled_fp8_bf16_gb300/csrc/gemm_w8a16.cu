@@ -98,19 +98,22 @@ __device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, 
   atomicCAS(err, 0, kDevErrW8A16 | site);
 }
 
-template <int COLS>
-__device__ __forceinline__ void store_col(__nv_bfloat16* __restrict__ C, int64_t ldc, int M, int m0, int n,
-                                          const float* acc) {
+__device__ __forceinline__ __nv_bfloat16 to_out(float v, __nv_bfloat16*) { return __float2bfloat16_rn(v); }
+__device__ __forceinline__ float to_out(float v, float*) { return v; }
+
+template <int COLS, class OutT>
+__device__ __forceinline__ void store_col(OutT* __restrict__ C, int64_t ldc, int M, int m0, int n, const float* acc) {
 #pragma unroll
   for (int j = 0; j < COLS; ++j) {
-    if (m0 + j < M) C[size_t(m0 + j) * ldc + n] = __float2bfloat16_rn(acc[j]);
+    if (m0 + j < M) C[size_t(m0 + j) * ldc + n] = to_out(acc[j], C);
   }
 }
 
-template <int TM>
+// OutT: __nv_bfloat16 (rounded to nearest even) or float (the accumulator as is).
+template <int TM, class OutT>
 __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
     w8a16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                 const void* __restrict__ scales, int fmt, __nv_bfloat16* __restrict__ C, int64_t ldc, int M,
+                 const void* __restrict__ scales, int fmt, OutT* __restrict__ C, int64_t ldc, int M,
                  int N, int K, int split, int* __restrict__ err) {
   using Q = Cfg<TM>;
   extern __shared__ uint8_t smem_raw[];
@@ -454,7 +457,7 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
   }
 }
 
-template <int TM>
+template <int TM, class OutT>
 cudaError_t launch_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t stream) {
   using Q = Cfg<TM>;
   static bool attr_done[64] = {};
@@ -462,7 +465,8 @@ cudaError_t launch_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   if (device < 64 && !attr_done[device]) {
-    e = cudaFuncSetAttribute(w8a16_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Q::kSmemBytes));
+    e = cudaFuncSetAttribute(w8a16_kernel<TM, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(Q::kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_done[device] = true;
   }
@@ -495,8 +499,8 @@ cudaError_t launch_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w8a16_kernel<TM>, p.tmW, p.tmX, p.scales, p.fmt,
-                            static_cast<__nv_bfloat16*>(p.C), p.ldc, p.M, p.N, p.K, split, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a16_kernel<TM, OutT>, p.tmW, p.tmX, p.scales, p.fmt, static_cast<OutT*>(p.C),
+                            p.ldc, p.M, p.N, p.K, split, p.err);
 }
 
 }  // namespace
@@ -509,11 +513,16 @@ int w8a16_pick_tile_m(int64_t M) {
 }
 
 cudaError_t launch_gemm_w8a16(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  if (p.out_f32) {
+    switch (p.tile_m) {
+      case 64: return launch_tm<64, float>(p, dev, stream);
+      case 128: return launch_tm<128, float>(p, dev, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (p.tile_m) {
-    case 16: return launch_tm<16>(p, dev, stream);
-    case 32: return launch_tm<32>(p, dev, stream);
-    case 64: return launch_tm<64>(p, dev, stream);
-    case 128: return launch_tm<128>(p, dev, stream);
+    case 64: return launch_tm<64, __nv_bfloat16>(p, dev, stream);
+    case 128: return launch_tm<128, __nv_bfloat16>(p, dev, stream);
     default: return cudaErrorInvalidValue;
   }
 }

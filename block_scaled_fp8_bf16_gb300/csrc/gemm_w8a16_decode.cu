@@ -119,10 +119,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, mbar_wait_sleep(bar, parity, abort_flag));
 }
 
-template <int TM>
+__device__ __forceinline__ __nv_bfloat16 to_out(float v, __nv_bfloat16*) { return __float2bfloat16_rn(v); }
+__device__ __forceinline__ float to_out(float v, float*) { return v; }
+
+// OutT: __nv_bfloat16 (rounded to nearest even) or float (the accumulator as is).
+template <int TM, class OutT>
 __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
     w8a16_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                        const void* __restrict__ scales, int fmt, __nv_bfloat16* __restrict__ C, int64_t ldc,
+                        const void* __restrict__ scales, int fmt, OutT* __restrict__ C, int64_t ldc,
                         int M, int N, int K, int split, int* __restrict__ err) {
   using Q = DecCfg<TM>;
   extern __shared__ uint8_t smem_raw[];
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
 #pragma unroll
         for (int r = 0; r < kMaxSplitK; ++r)
           if (r < split) sum += v[r];
-        C[size_t(m) * ldc + n_out] = __float2bfloat16_rn(sum);
+        C[size_t(m) * ldc + n_out] = to_out(sum, C);
       }
       __syncwarp();
       if (lane == 0) {
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
         const int n = nt * BN + row;
 #pragma unroll
         for (int m = 0; m < TM; ++m)
-          if (m < M) C[size_t(m) * ldc + n] = __float2bfloat16_rn(acc[m]);
+          if (m < M) C[size_t(m) * ldc + n] = to_out(acc[m], C);
         continue;
       }
       // ---- cluster reduction: every rank publishes its partial of tile q in
@@ -498,7 +502,8 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
   if (split > 1) cluster_sync();   // no CTA leaves while a peer may still read its shared memory
 }
 
-// Largest number of clusters of `split` CTAs that can be resident at once.
+// Largest number of clusters of `split` CTAs that can be resident at once
+// (both output types use the same resources).
 template <int TM>
 int max_active_clusters(int split, const DeviceInfo& dev) {
   using Q = DecCfg<TM>;
@@ -519,7 +524,7 @@ int max_active_clusters(int split, const DeviceInfo& dev) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, w8a16_decode_kernel<TM>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, w8a16_decode_kernel<TM, __nv_bfloat16>, &cfg) != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
       n = dev.num_sms / split;
     }
@@ -528,7 +533,7 @@ int max_active_clusters(int split, const DeviceInfo& dev) {
   return slot;
 }
 
-template <int TM>
+template <int TM, class OutT>
 cudaError_t launch_decode_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t stream) {
   using Q = DecCfg<TM>;
   static bool attr_done[64] = {};
@@ -536,7 +541,7 @@ cudaError_t launch_decode_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cuda
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   if (device < 64 && !attr_done[device]) {
-    e = cudaFuncSetAttribute(w8a16_decode_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(w8a16_decode_kernel<TM, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(Q::kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_done[device] = true;
@@ -558,8 +563,8 @@ cudaError_t launch_decode_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cuda
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w8a16_decode_kernel<TM>, p.tmW, p.tmX, p.scales, p.fmt,
-                            static_cast<__nv_bfloat16*>(p.C), p.ldc, p.M, p.N, p.K, plan.split, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a16_decode_kernel<TM, OutT>, p.tmW, p.tmX, p.scales, p.fmt,
+                            static_cast<OutT*>(p.C), p.ldc, p.M, p.N, p.K, plan.split, p.err);
 }
 
 }  // namespace
@@ -567,8 +572,10 @@ cudaError_t launch_decode_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cuda
 cudaError_t launch_w8a16_decode(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t stream) {
   if (p.M > p.tile_m) return cudaErrorInvalidValue;
   switch (p.tile_m) {
-    case 16: return launch_decode_tm<16>(p, dev, stream);
-    case 32: return launch_decode_tm<32>(p, dev, stream);
+    case 16: return p.out_f32 ? launch_decode_tm<16, float>(p, dev, stream)
+                              : launch_decode_tm<16, __nv_bfloat16>(p, dev, stream);
+    case 32: return p.out_f32 ? launch_decode_tm<32, float>(p, dev, stream)
+                              : launch_decode_tm<32, __nv_bfloat16>(p, dev, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -85,6 +85,12 @@ __device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, 
   atomicCAS(err, 0, kDevErrW8A8 | site);
 }
 
+__device__ __forceinline__ void store_row64(float* dst, const float* acc) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < kColsPerThread / 4; ++i) d[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+}
+
 __device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* acc) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -98,10 +104,12 @@ __device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* acc
   }
 }
 
+// OutT: __nv_bfloat16 (rounded to nearest even) or float (the accumulator as is).
+template <class OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmAs, const float* __restrict__ Bs,
-                __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N, int K, int split,
+                OutT* __restrict__ C, int64_t ldc, int M, int N, int K, int split,
                 int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -359,17 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
-  // Enough 256x256 tiles to keep most CTA pairs busy: the pair kernel.
-  if (p.M > kW8A8TileM && 2 * w8a8_pair_tiles(p.M, p.N) >= dev.num_sms / 2) return launch_gemm_w8a8_pair(p, dev, stream);
+template <class OutT>
+cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
   static bool attr_done[64] = {};
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   if (device < 64 && !attr_done[device]) {
-    e = cudaFuncSetAttribute(w8a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    e = cudaFuncSetAttribute(w8a8_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_done[device] = true;
   }
@@ -402,8 +407,16 @@ cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaS
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_kernel, p.tmA, p.tmB, p.tmAs, p.Bs,
-                            static_cast<__nv_bfloat16*>(p.C), p.ldc, p.M, p.N, p.K, split, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a8_kernel<OutT>, p.tmA, p.tmB, p.tmAs, p.Bs, static_cast<OutT*>(p.C), p.ldc,
+                            p.M, p.N, p.K, split, p.err);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  // Enough 256x256 tiles to keep most CTA pairs busy: the pair kernel.
+  if (p.M > kW8A8TileM && 2 * w8a8_pair_tiles(p.M, p.N) >= dev.num_sms / 2) return launch_gemm_w8a8_pair(p, dev, stream);
+  return p.out_f32 ? launch_single<float>(p, dev, stream) : launch_single<__nv_bfloat16>(p, dev, stream);
 }
 
 }  // namespace fp8blk

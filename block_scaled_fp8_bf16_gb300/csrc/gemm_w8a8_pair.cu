@@ -124,6 +124,25 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   }
 }
 
+// 16 bytes of output row r, chunk c of 128-byte box b of a warp's 128
+// columns: eight bf16 (acc pairs 32b + 4c ..) or four float32 (16b + 2c ..).
+template <bool F32>
+__device__ __forceinline__ uint4 out_chunk(const float2* acc, int b, int c) {
+  uint4 v;
+  if constexpr (F32) {
+    const float2 p = acc[b * 16 + 2 * c], q = acc[b * 16 + 2 * c + 1];
+    v = make_uint4(__float_as_uint(p.x), __float_as_uint(p.y), __float_as_uint(q.x), __float_as_uint(q.y));
+  } else {
+    const float2* a = acc + b * 32 + 4 * c;
+    v.x = pack_bf16x2(a[0].x, a[0].y);
+    v.y = pack_bf16x2(a[1].x, a[1].y);
+    v.z = pack_bf16x2(a[2].x, a[2].y);
+    v.w = pack_bf16x2(a[3].x, a[3].y);
+  }
+  return v;
+}
+
+template <bool F32>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmAsG, const __grid_constant__ CUtensorMap tmC,
@@ -366,30 +385,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (ok && y < M && col_ok) {
-        // Two 32 x 64 boxes; chunk c (8 columns) of row r sits at 16-byte
-        // position c ^ (r & 7) of the row's 128 bytes (128-byte swizzle).
-        if (lane == 0) bulk_wait_group_read0();   // the previous tile's stores have left the staging buffers
-        __syncwarp();
+        // The warp's 32 x 128 block leaves as 128-byte-wide boxes (64 bf16 or
+        // 32 float32 columns), kBoxesPerWarp at a time through the staging
+        // boxes; chunk c (16 bytes) of row r sits at 16-byte position
+        // c ^ (r & 7) of the row (128-byte swizzle).
+        constexpr int kBoxCols = F32 ? 32 : 64;
+        constexpr int kRounds = kCols / kBoxCols / kBoxesPerWarp;
 #pragma unroll
-        for (int h = 0; h < kBoxesPerWarp; ++h) {
-          uint8_t* dst = stg + h * kStageC + lane * 128;
+        for (int r = 0; r < kRounds; ++r) {
+          if (lane == 0) bulk_wait_group_read0();   // earlier stores have left the staging boxes
+          __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float2* a = acc + h * 32 + 4 * c;
-            uint4 v;
-            v.x = pack_bf16x2(a[0].x, a[0].y);
-            v.y = pack_bf16x2(a[1].x, a[1].y);
-            v.z = pack_bf16x2(a[2].x, a[2].y);
-            v.w = pack_bf16x2(a[3].x, a[3].y);
-            *reinterpret_cast<uint4*>(dst + ((c ^ (lane & 7)) << 4)) = v;
+          for (int h = 0; h < kBoxesPerWarp; ++h) {
+            uint8_t* dst = stg + h * kStageC + lane * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(dst + ((c ^ (lane & 7)) << 4)) = out_chunk<F32>(acc, r * kBoxesPerWarp + h, c);
           }
-        }
-        fence_async_shared();   // generic-proxy writes become visible to the TMA engine
-        __syncwarp();
-        if (lane == 0) {
+          fence_async_shared();   // generic-proxy writes become visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
 #pragma unroll
-          for (int h = 0; h < kBoxesPerWarp; ++h) tma_store_2d(&tmC, stg + h * kStageC, n + h * 64, y);
-          bulk_commit_group();
+            for (int h = 0; h < kBoxesPerWarp; ++h)
+              tma_store_2d(&tmC, stg + h * kStageC, n + (r * kBoxesPerWarp + h) * kBoxCols, y);
+            bulk_commit_group();
+          }
         }
       }
     }
@@ -412,7 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int w8a8_pair_tiles(int M, int N) { return ((M + 2 * TM - 1) / (2 * TM)) * ((N + PN - 1) / PN); }
 
-cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+namespace {
+
+template <bool F32>
+cudaError_t launch_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
   static bool attr_done[64] = {};
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
@@ -421,10 +444,10 @@ cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, 
     // The setmaxnreg split assumes the launch register count; refuse to run
     // any build where it differs.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, w8a8_pair_kernel);
+    e = cudaFuncGetAttributes(&fa, w8a8_pair_kernel<F32>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(w8a8_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    e = cudaFuncSetAttribute(w8a8_pair_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_done[device] = true;
   }
@@ -445,7 +468,13 @@ cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel, p.tmA, p.tmB, p.tmAsG, p.tmC, p.Bs, p.M, p.N, p.K, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel<F32>, p.tmA, p.tmB, p.tmAsG, p.tmC, p.Bs, p.M, p.N, p.K, p.err);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  return p.out_f32 ? launch_pair<true>(p, dev, stream) : launch_pair<false>(p, dev, stream);
 }
 
 }  // namespace fp8blk

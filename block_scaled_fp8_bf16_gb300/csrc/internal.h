@@ -76,12 +76,13 @@ struct GemmW8A8Args {
   CUtensorMap tmB;    // e4m3 [N, K], box {128 (K), kW8A8TileN (N)}, 128B swizzle
   CUtensorMap tmAs;   // fp32 [K/128][lds] read as {M, K/128}, box {128, 1}, no swizzle
   CUtensorMap tmAsG;  // the same scales, box {128, 8}: eight K blocks per copy (pair kernel)
-  CUtensorMap tmC;    // bf16 [M, N] pitch ldc, box {64 (N), 32 (M)}, 128B swizzle (pair kernel's stores)
+  CUtensorMap tmC;    // C [M, N] pitch ldc, box {128 bytes of N, 32 (M)}, 128B swizzle (pair kernel's stores)
   const float* Bs;    // [N/128][K/128]
   void* C;            // bf16 [M, ldc]
   int64_t ldc;
   int M, N, K;
   bool pdl;           // launch with programmatic stream serialisation
+  bool out_f32;       // C is float32 (ldc in float32 elements), else bf16
   int* err;
 };
 constexpr int kW8A8TileM = 128;
@@ -103,6 +104,7 @@ struct GemmW8A16Args {
   int M, N, K;
   int tile_m;         // token tile (MMA N): 16, 32, 64 or 128
   bool pdl;           // launch with programmatic stream serialisation
+  bool out_f32;       // C is float32 (ldc in float32 elements), else bf16
   int* err;
 };
 constexpr int kW8A16TileN = 128;

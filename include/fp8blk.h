@@ -108,6 +108,18 @@ typedef struct {
  */
 #define FP8BLK_FLAG_PDL 1u
 
+/*
+ * FP8BLK_FLAG_OUT_F32  C is float32 instead of bf16: the FP32 accumulator
+ *   is stored as it is, with no rounding to bf16, for outputs that are summed
+ *   further in FP32 (the K-sharded, row-parallel form of the layer, whose
+ *   partial outputs are reduced across devices before the final rounding;
+ *   "SM70 FP8 block-32 kernels", which keeps row-parallel outputs in FP32).
+ *   ldc then counts float32 elements and ldc*4 % 16 == 0.  The accumulation
+ *   is the same as for bf16 output: rounding the float32 result to bf16
+ *   (nearest even) gives exactly the bf16 result of the same call.
+ */
+#define FP8BLK_FLAG_OUT_F32 2u
+
 /* ------------------------------------------------------------------------ */
 /* Hot path                                                                 */
 /* ------------------------------------------------------------------------ */
@@ -146,7 +158,8 @@ FP8BLK_API fp8blk_status fp8blk_quant_act(const void* x_bf16, int64_t M, int64_t
  *  a_scales  [K/128][lds] float32 (as written by fp8blk_quant_act).
  *  b_e4m3    [N, K] e4m3 weights, K contiguous, row pitch ldb bytes.
  *  b_scales  [N/128][K/128] float32, row-major, packed.
- *  c_bf16    [M, N] bf16 out, row pitch ldc elements (ldc*2 % 16 == 0).
+ *  c_bf16    [M, N] bf16 out, row pitch ldc elements (ldc*2 % 16 == 0);
+ *            float32 with FP8BLK_FLAG_OUT_F32 (ldc*4 % 16 == 0).
  *  N % 128 == 0, K % 128 == 0, M >= 0 (M == 0 is a no-op).
  *  Weights are assumed finite (see fp8blk_validate_weights).
  *  flags     FP8BLK_FLAG_* (unknown bits: FP8BLK_ERR_INVALID_ARG).
@@ -176,7 +189,8 @@ FP8BLK_API fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda,
  *
  *  x_bf16  [M, K] bf16, row pitch ldx elements (ldx*2 % 16 == 0).
  *  b_e4m3  [N, K] e4m3, row pitch ldb bytes (ldb % 16 == 0).
- *  c_bf16  [M, N] bf16 out, row pitch ldc elements.
+ *  c_bf16  [M, N] bf16 out, row pitch ldc elements (ldc*2 % 16 == 0);
+ *          float32 with FP8BLK_FLAG_OUT_F32 (ldc*4 % 16 == 0).
  *  M == 0 is a no-op.  Scales outside [-14, 7] are outside the contract.
  *  flags   FP8BLK_FLAG_* (unknown bits: FP8BLK_ERR_INVALID_ARG).
  *  M <= 32 runs the decode-size kernel (weight stream split over clusters of

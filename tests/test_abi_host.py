@@ -105,8 +105,12 @@ def test_w8a8_argument_errors(fp8blk):
     assert call_w8a8(lib, lds=18) == 3
     assert call_w8a8(lib, ldc=260) == 3
     assert call_w8a8(lib, M=1 << 31) == 2
-    assert call_w8a8(lib, flags=2) == 1             # unknown launch flag
+    assert call_w8a8(lib, flags=4) == 1             # unknown launch flag
     assert call_w8a8(lib, M=0, flags=1) == 0        # FP8BLK_FLAG_PDL is known
+    assert call_w8a8(lib, M=0, flags=2) == 0        # FP8BLK_FLAG_OUT_F32 is known
+    assert call_w8a8(lib, ldc=258, flags=2) == 3    # float32 rows need ldc * 4 % 16 == 0
+    assert call_w8a8(lib, ldc=260) == 3             # bf16 rows need ldc * 2 % 16 == 0 ...
+    assert call_w8a8(lib, ldc=260, flags=2) != 3    # ... which float32 rows of the same pitch meet
 
 
 def test_w8a16_and_gemv_argument_errors(fp8blk):
