@@ -38,6 +38,10 @@ tests/test_oracle_gemm.py):
                          inputs, one-hot rows, unit-scale reduction.
   gemm_w8a16_f32scale    pinned: Fraction brute force on tiny inputs.
   gemm_w8a16_ue8m0       pinned: Fraction brute force on tiny inputs.
+  gemm_w8a8_grouped      pinned: one group reduces to gemm_w8a8; every row
+                         equals the single-weight product with its group's
+                         weights (int64 brute force on tiny inputs); row-block
+                         permutation invariance; padding rows stay untouched.
   End-to-end output numbers are "parity unpinned" against the pages: no page
   prints a per-element worked example of the product.
 """
@@ -49,7 +53,7 @@ __all__ = [
     "E4M3_MAX", "E4M3_NAN_CODES", "e4m3_decode", "e4m3_encode", "e4m3_finite_values",
     "bf16_bits_to_f64", "f64_to_bf16_bits", "fp32_div", "ue8m0_value",
     "quant_act_1x128", "quant_weight_128x128",
-    "gemm_w8a8", "gemm_w8a16_f32scale", "gemm_w8a16_ue8m0",
+    "gemm_w8a8", "gemm_w8a16_f32scale", "gemm_w8a16_ue8m0", "gemm_w8a8_grouped",
     "gemm_w8a8_rows", "gemm_w8a16_f32scale_rows", "gemm_w8a16_ue8m0_rows",
     "UE8M0_EMIN", "UE8M0_EMAX", "UE8M0_BIAS",
 ]
@@ -266,6 +270,28 @@ def gemm_w8a8_rows(a_codes, a_scales, b_codes, b_scales, rows=None) -> np.ndarra
 
 def gemm_w8a8(a_codes, a_scales, b_codes, b_scales) -> np.ndarray:
     return gemm_w8a8_rows(a_codes, a_scales, b_codes, b_scales, None)
+
+
+def gemm_w8a8_grouped(a_codes, a_scales, b_codes, b_scales, row_group, fill=np.nan) -> np.ndarray:
+    """Grouped (mixture-of-experts) form of the W8A8 product: row m of A is
+    multiplied by the weights of group row_group[m] (one expert per row, the
+    rows of each expert stored contiguously), with the same block scaling as
+    gemm_w8a8 [P1 "The fix"].  Rows with row_group[m] < 0 are padding and
+    get `fill` (the GPU leaves them untouched).
+
+    b_codes [G, N, K] uint8, b_scales [G, N/128, K/128] float32,
+    row_group [M] int; other arguments as gemm_w8a8.
+    """
+    A = np.asarray(a_codes)
+    g = np.asarray(row_group, dtype=np.int64)
+    M = A.shape[0]
+    B = np.asarray(b_codes)
+    C = np.full((M, B.shape[1]), fill, dtype=np.float64)
+    for e in range(B.shape[0]):
+        rows = np.nonzero(g == e)[0]
+        if rows.size:
+            C[rows] = gemm_w8a8_rows(A, a_scales, B[e], np.asarray(b_scales)[e], rows)
+    return C
 
 
 def gemm_w8a16_f32scale_rows(x_bf16_bits, b_codes, b_scales, rows=None) -> np.ndarray:

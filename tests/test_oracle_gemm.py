@@ -133,3 +133,54 @@ def test_w8a16_unit_scale_reduces_to_plain_matmul():
     # UE8M0 with every byte 127 (scale 1) is the same product
     e = np.full((N // 32, K // 32), 127, dtype=np.uint8)
     assert np.allclose(O.gemm_w8a16_ue8m0(x, b, e), ref.numpy(), rtol=1e-14, atol=1e-12)
+
+
+# ---------------------------------------------------------------- grouped (mixture-of-experts) form
+
+def tiny_grouped(seed, G=3, rows_per_group=(2, 3, 1), N=256, K=256):
+    M = sum(rows_per_group)
+    x = synth.activations(seed, M, K, outliers=True)
+    a, As = O.quant_act_1x128(x)
+    bs, Bss = [], []
+    for e in range(G):
+        b, Bs = O.quant_weight_128x128(synth.weights_bf16(seed * 10 + e, N, K))
+        bs.append(b)
+        Bss.append(Bs * np.float32(1.0 + e))     # clearly different scales per expert
+    g = np.repeat(np.arange(G), rows_per_group)
+    return a, As, np.stack(bs), np.stack(Bss), g
+
+
+def test_grouped_single_group_is_plain_w8a8():
+    a, As, b, Bs = tiny_w8a8(6, M=5)
+    C = O.gemm_w8a8_grouped(a, As, b[None], Bs[None], np.zeros(5, dtype=np.int64))
+    assert np.array_equal(C, O.gemm_w8a8(a, As, b, Bs))
+
+
+def test_grouped_rows_against_int64_brute_force():
+    """Every row equals the exact product with its own expert's weights."""
+    a, As, b, Bs, g = tiny_grouped(7)
+    C = O.gemm_w8a8_grouped(a, As, b, Bs, g)
+    ai = as_int9(a)
+    for m in range(a.shape[0]):
+        e = int(g[m])
+        bi = as_int9(b[e])
+        for n in (0, 100, 128, 255):
+            tot = Fraction(0)
+            for kb in range(a.shape[1] // 128):
+                p = int(np.dot(ai[m, kb * 128:(kb + 1) * 128], bi[n, kb * 128:(kb + 1) * 128]))
+                tot += Fraction(p, 2 ** 18) * Fraction(float(As[kb, m])) * Fraction(float(Bs[e, n // 128, kb]))
+            assert abs(C[m, n] - float(tot)) <= 1e-13 * abs(float(tot)) + 1e-300, (m, n)
+
+
+def test_grouped_row_permutation_and_padding():
+    a, As, b, Bs, g = tiny_grouped(8)
+    C = O.gemm_w8a8_grouped(a, As, b, Bs, g)
+    perm = np.array([5, 0, 3, 1, 4, 2])
+    Cp = O.gemm_w8a8_grouped(a[perm], As[:, perm], b, Bs, g[perm])
+    assert np.array_equal(Cp, C[perm])
+    g2 = g.copy()
+    g2[[1, 4]] = -1                               # padding rows
+    C2 = O.gemm_w8a8_grouped(a, As, b, Bs, g2, fill=-7.0)
+    assert np.all(C2[[1, 4]] == -7.0)
+    keep = [0, 2, 3, 5]
+    assert np.array_equal(C2[keep], C[keep])
