@@ -410,8 +410,9 @@ def reference_arm(args, world, rank):
 
 # ---------------------------------------------------------------- sweep
 
-def sweep(out_path):
-    """Times every workload shape with CUDA-graph replays over rotated copies."""
+def sweep(out_path, kinds=None):
+    """Times every workload shape with CUDA-graph replays over rotated copies
+    (kinds: optional subset of "w8a8", "grouped", "w8a16")."""
     import torch
 
     import block_scaled_fp8_bf16_gb300 as fp8blk
@@ -466,6 +467,8 @@ def sweep(out_path):
     for M in (256, 2048, 8192):
         for N, K in ((7168, 2048), (2048, 7168), (18432, 7168), (7168, 18432)):
             w8a8.append((M, N, K))
+    if kinds is not None and "w8a8" not in kinds:
+        w8a8 = []
     PDL = fp8blk.FLAG_PDL
     for M, N, K in w8a8:
         per = M * K * 3 + N * K + M * N * 2
@@ -486,6 +489,26 @@ def sweep(out_path):
         record("quant_act", M, 0, K, graph_time(qcalls), 0.0, 3 * M * K + (K // 128) * M * 4, fp8_peak)
         del sets
         torch.cuda.empty_cache()
+    # Grouped (mixture-of-experts) W8A8: G experts with the same number of
+    # 128-row tiles each, N x K weights per expert.
+    grouped = [(8, 512, 4096, 4096), (32, 256, 2048, 7168), (64, 128, 7168, 2048)]
+    if kinds is not None and "grouped" not in kinds:
+        grouped = []
+    for G, per_group, N, K in grouped:
+        M = G * per_group
+        xg = tg.activations(1, M, K)
+        a, sc = fp8blk.quant_act(xg)
+        ws = [fp8blk.quant_weight(tg.weights_bf16(1 + e, N, K)) for e in range(G)]
+        b = torch.stack([w[0] for w in ws])
+        bs = torch.stack([w[1] for w in ws])
+        del ws
+        rg = torch.arange(G, dtype=torch.int32, device="cuda").repeat_interleave(per_group)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        calls = [lambda: fp8blk.fp8blk_gemm_w8a8_grouped(a, sc, b, bs, rg, c)]
+        byt = M * K + (K // 128) * M * 4 + G * N * K + G * (N // 128) * (K // 128) * 4 + 2 * M * N
+        record(f"w8a8_grouped_G{G}", M, N, K, graph_time(calls * 4), 2.0 * M * N * K, byt, fp8_peak)
+        del a, sc, b, bs, c
+        torch.cuda.empty_cache()
     # W8A16 fp32-scale decode and UE8M0
     w8a16 = []
     for N, K in ((4096, 4096), (28672, 4096), (4096, 14336)):
@@ -494,6 +517,8 @@ def sweep(out_path):
     for N, K in ((2048, 7168), (7168, 2048)):
         for M in (1, 4, 16, 32, 128, 512, 4096):
             w8a16.append((1, M, N, K))
+    if kinds is not None and "w8a16" not in kinds:
+        w8a16 = []
     for fmt, M, N, K in w8a16:
         per = N * K + M * K * 2 + M * N * 2
         R = _rot_copies(per, l2, cap=64)
@@ -565,6 +590,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sweep", default=None, metavar="OUT.json",
                     help="also time every workload shape and write the table to OUT.json")
+    ap.add_argument("--sweep-kinds", default=None,
+                    help="comma list restricting --sweep to some of: w8a8, grouped, w8a16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None, help="run one configuration untimed (w8a8:M,N,K | quant:M,K | "
                                                   "w8a16:M,N,K,fmt) for profiling")
@@ -592,7 +619,7 @@ def main():
             line["cpu_baseline"] = cpu_baseline()
         if args.sweep:
             os.makedirs(os.path.dirname(os.path.abspath(args.sweep)), exist_ok=True)
-            sweep(args.sweep)
+            sweep(args.sweep, None if args.sweep_kinds is None else set(args.sweep_kinds.split(",")))
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -45,6 +45,8 @@ _U32 = ctypes.c_uint32
 EXPORTS = {
     "fp8blk_quant_act": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
     "fp8blk_gemm_w8a8": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _U32, _P]),
+    "fp8blk_gemm_w8a8_grouped": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _I64, _U32,
+                                         _P]),
     "fp8blk_gemm_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_gemv_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_quant_weight": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P]),
@@ -161,6 +163,22 @@ def fp8blk_gemm_w8a8(a, a_scales, b, b_scales, c, stream=None, flags=0):
                                 _ptr(c), _ld(c), M, N, K, _out_flags(c, flags), _stream(stream)), "fp8blk_gemm_w8a8")
 
 
+def fp8blk_gemm_w8a8_grouped(a, a_scales, b, b_scales, row_group, c, stream=None, flags=0):
+    """Grouped (mixture-of-experts) W8A8: row m uses the weights of group
+    row_group[m].  b [G, N, K] e4m3 (K contiguous), b_scales [G, N/128, K/128],
+    row_group int32 [M] (constant per aligned 128-row block, negative = padding)."""
+    import torch
+    a, b = _bytes_tensor(a), _bytes_tensor(b)
+    _expect(row_group, (torch.int32,), "row_group")
+    M, K = a.shape
+    G, N, Kb = b.shape
+    if Kb != K or b.stride(2) != 1 or b.stride(0) != N * b.stride(1):
+        raise ValueError("b must be [G, N, K] with K contiguous and the groups stacked at one row pitch")
+    _check(_L().fp8blk_gemm_w8a8_grouped(_ptr(a), _ld(a), _ptr(a_scales), _ld(a_scales), _ptr(b), b.stride(1),
+                                        _ptr(b_scales), _ptr(row_group), G, _ptr(c), _ld(c), M, N, K,
+                                        _out_flags(c, flags), _stream(stream)), "fp8blk_gemm_w8a8_grouped")
+
+
 def fp8blk_gemm_w8a16(x, b, b_scales, fmt, c, stream=None, flags=0):
     """C[M, N] bf16 = x[M, K] bf16 x b[N, K] e4m3 with fp32 128x128 or UE8M0 32x32 scales."""
     b = _bytes_tensor(b)
@@ -253,6 +271,14 @@ def gemm_w8a8(a, a_scales, b, b_scales, out=None, stream=None, flags=0, out_dtyp
     if out is None:
         out = torch.empty((a.shape[0], b.shape[0]), dtype=out_dtype or torch.bfloat16, device=a.device)
     fp8blk_gemm_w8a8(a, a_scales, b, b_scales, out, stream, flags)
+    return out
+
+
+def gemm_w8a8_grouped(a, a_scales, b, b_scales, row_group, out=None, stream=None, flags=0, out_dtype=None):
+    import torch
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[1]), dtype=out_dtype or torch.bfloat16, device=a.device)
+    fp8blk_gemm_w8a8_grouped(a, a_scales, b, b_scales, row_group, out, stream, flags)
     return out
 
 

@@ -206,6 +206,67 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   return cuda_status(decode ? launch_w8a16_decode(p, dev, s) : launch_gemm_w8a16(p, dev, s));
 }
 
+// Shared by the plain and the grouped W8A8 entry points; G == 0 means plain.
+fp8blk_status run_w8a8(const void* a_e4m3, int64_t lda, const float* a_scales, int64_t lds, const void* b_e4m3,
+                       int64_t ldb, const float* b_scales, const int32_t* row_group, int64_t G, void* c_bf16,
+                       int64_t ldc, int64_t M, int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || G < 0 || (flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
+  if (M > kIntMax || N > kIntMax || K > kIntMax || G * N > kIntMax) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
+  if (G > 0 && M % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return FP8BLK_OK;
+  if (!c_bf16) return FP8BLK_ERR_INVALID_ARG;
+  if (K > 0 && (!a_e4m3 || !a_scales || !b_e4m3 || !b_scales)) return FP8BLK_ERR_INVALID_ARG;
+  if (G > 0 && K > 0 && !row_group) return FP8BLK_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldc < N || lds < M) return FP8BLK_ERR_INVALID_ARG;
+  if ((a_e4m3 && !aligned16(a_e4m3)) || (a_scales && !aligned16(a_scales)) || (b_e4m3 && !aligned16(b_e4m3)) ||
+      (b_scales && !aligned16(b_scales)) || !aligned16(c_bf16) ||
+      (row_group && (reinterpret_cast<uintptr_t>(row_group) & 3u) != 0))
+    return FP8BLK_ERR_MISALIGNED;
+  const int64_t c_elem = (flags & FP8BLK_FLAG_OUT_F32) ? 4 : 2;
+  if (lda % 16 != 0 || ldb % 16 != 0 || (ldc * c_elem) % 16 != 0 || lds % 4 != 0) return FP8BLK_ERR_MISALIGNED;
+  DeviceInfo dev;
+  fp8blk_status st = device_info(dev);
+  if (st != FP8BLK_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
+  if (K == 0) return zero_output(c_bf16, ldc, M, N, f32 ? 4 : 2, s);
+  const int64_t b_rows = G > 0 ? G * N : N;
+  GemmW8A8Args p;
+  st = make_map(p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_e4m3, uint64_t(K), uint64_t(M), uint64_t(lda), 128,
+                kW8A8TileM);
+  if (st != FP8BLK_OK) return st;
+  st = make_map(p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_e4m3, uint64_t(K), uint64_t(b_rows), uint64_t(ldb), 128,
+                kW8A8TileN);
+  if (st != FP8BLK_OK) return st;
+  // Scales are read through the full pitch (lds >= M, a multiple of 4, so
+  // 16-byte rows); rows past M are never stored.
+  st = make_map(p.tmAs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scales, uint64_t(lds), uint64_t(K / 128),
+                uint64_t(lds) * 4, kW8A8TileM, 1, false);
+  if (st != FP8BLK_OK) return st;
+  st = make_map(p.tmAsG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scales, uint64_t(lds), uint64_t(K / 128),
+                uint64_t(lds) * 4, kW8A8TileM, 8, false);
+  if (st != FP8BLK_OK) return st;
+  // Output boxes of 32 rows x 128 bytes (64 bf16 or 32 float32 columns).
+  if (f32)
+    st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c_bf16, uint64_t(N), uint64_t(M), uint64_t(ldc) * 4, 32, 32);
+  else
+    st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c_bf16, uint64_t(N), uint64_t(M), uint64_t(ldc) * 2, 64, 32);
+  if (st != FP8BLK_OK) return st;
+  p.Bs = b_scales;
+  p.C = c_bf16;
+  p.ldc = ldc;
+  p.M = int(M);
+  p.N = int(N);
+  p.K = int(K);
+  p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
+  p.out_f32 = f32;
+  p.row_group = G > 0 ? row_group : nullptr;
+  p.groups = G > 0 ? int(G) : 1;
+  p.err = dev.err_word;
+  return cuda_status(launch_gemm_w8a8(p, dev, s));
+}
+
 }  // namespace
 }  // namespace fp8blk
 
@@ -232,55 +293,17 @@ fp8blk_status fp8blk_quant_act(const void* x_bf16, int64_t M, int64_t K, int64_t
 fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda, const float* a_scales, int64_t lds,
                                const void* b_e4m3, int64_t ldb, const float* b_scales, void* c_bf16, int64_t ldc,
                                int64_t M, int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
-  if (M < 0 || N < 0 || K < 0 || (flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
-  if (N % 128 != 0 || K % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
-  if (M > kIntMax || N > kIntMax || K > kIntMax) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
-  if (M == 0 || N == 0) return FP8BLK_OK;
-  if (!c_bf16) return FP8BLK_ERR_INVALID_ARG;
-  if (K > 0 && (!a_e4m3 || !a_scales || !b_e4m3 || !b_scales)) return FP8BLK_ERR_INVALID_ARG;
-  if (lda < K || ldb < K || ldc < N || lds < M) return FP8BLK_ERR_INVALID_ARG;
-  if ((a_e4m3 && !aligned16(a_e4m3)) || (a_scales && !aligned16(a_scales)) || (b_e4m3 && !aligned16(b_e4m3)) ||
-      (b_scales && !aligned16(b_scales)) || !aligned16(c_bf16))
-    return FP8BLK_ERR_MISALIGNED;
-  const int64_t c_elem = (flags & FP8BLK_FLAG_OUT_F32) ? 4 : 2;
-  if (lda % 16 != 0 || ldb % 16 != 0 || (ldc * c_elem) % 16 != 0 || lds % 4 != 0) return FP8BLK_ERR_MISALIGNED;
-  DeviceInfo dev;
-  fp8blk_status st = device_info(dev);
-  if (st != FP8BLK_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
-  if (K == 0) return zero_output(c_bf16, ldc, M, N, f32 ? 4 : 2, s);
-  GemmW8A8Args p;
-  st = make_map(p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_e4m3, uint64_t(K), uint64_t(M), uint64_t(lda), 128,
-                kW8A8TileM);
-  if (st != FP8BLK_OK) return st;
-  st = make_map(p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_e4m3, uint64_t(K), uint64_t(N), uint64_t(ldb), 128,
-                kW8A8TileN);
-  if (st != FP8BLK_OK) return st;
-  // Scales are read through the full pitch (lds >= M, a multiple of 4, so
-  // 16-byte rows); rows past M are never stored.
-  st = make_map(p.tmAs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scales, uint64_t(lds), uint64_t(K / 128),
-                uint64_t(lds) * 4, kW8A8TileM, 1, false);
-  if (st != FP8BLK_OK) return st;
-  st = make_map(p.tmAsG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scales, uint64_t(lds), uint64_t(K / 128),
-                uint64_t(lds) * 4, kW8A8TileM, 8, false);
-  if (st != FP8BLK_OK) return st;
-  // Output boxes of 32 rows x 128 bytes (64 bf16 or 32 float32 columns).
-  if (f32)
-    st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c_bf16, uint64_t(N), uint64_t(M), uint64_t(ldc) * 4, 32, 32);
-  else
-    st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c_bf16, uint64_t(N), uint64_t(M), uint64_t(ldc) * 2, 64, 32);
-  if (st != FP8BLK_OK) return st;
-  p.Bs = b_scales;
-  p.C = c_bf16;
-  p.ldc = ldc;
-  p.M = int(M);
-  p.N = int(N);
-  p.K = int(K);
-  p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
-  p.out_f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
-  p.err = dev.err_word;
-  return cuda_status(launch_gemm_w8a8(p, dev, s));
+  return run_w8a8(a_e4m3, lda, a_scales, lds, b_e4m3, ldb, b_scales, nullptr, 0, c_bf16, ldc, M, N, K, flags,
+                  stream);
+}
+
+fp8blk_status fp8blk_gemm_w8a8_grouped(const void* a_e4m3, int64_t lda, const float* a_scales, int64_t lds,
+                                       const void* b_e4m3, int64_t ldb, const float* b_scales,
+                                       const int32_t* row_group, int64_t G, void* c_bf16, int64_t ldc, int64_t M,
+                                       int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
+  if (G < 1) return FP8BLK_ERR_INVALID_ARG;
+  return run_w8a8(a_e4m3, lda, a_scales, lds, b_e4m3, ldb, b_scales, row_group, G, c_bf16, ldc, M, N, K, flags,
+                  stream);
 }
 
 fp8blk_status fp8blk_gemm_w8a16(const void* x_bf16, int64_t ldx, const void* b_e4m3, int64_t ldb,

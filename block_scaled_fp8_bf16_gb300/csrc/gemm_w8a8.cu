@@ -37,6 +37,14 @@
 // over a thread-block cluster of 2..8 CTAs; the partial accumulators are
 // summed through distributed shared memory in rank order (no global
 // workspace), and rank 0 writes C.
+//
+// Grouped (mixture-of-experts) form: with row_group != nullptr the rows of A
+// and C are split into groups (experts) stored contiguously in 128-row tiles,
+// row_group[m] naming the group of row m (the same for the 128 rows of a
+// tile; negative for a padding tile, which is skipped and left untouched).
+// Tile (mt, nt) then multiplies with rows g*N + nt*128 of the stacked
+// weights [G*N, K] and scales Bs[g][nt][kb]; every role reads the tile's
+// group from row_group and skips the same tiles.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -110,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmAs, const float* __restrict__ Bs,
                 OutT* __restrict__ C, int64_t ldc, int M, int N, int K, int split,
-                int* __restrict__ err) {
+                const int* __restrict__ row_group, int G, int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -136,6 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_clusters = gridDim.x / split;
   const int kb_begin = (kblocks * rank) / split;
   const int kb_end = (kblocks * (rank + 1)) / split;
+  // Group of row tile mt (0 when ungrouped); outside [0, G) the tile is skipped.
+  auto group_of = [&](int mt) -> int { return row_group != nullptr ? __ldg(row_group + size_t(mt) * BM) : 0; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -174,7 +184,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && row_group != nullptr) {
+      // Grouped: the tile's group (an activation-side input) decides which
+      // weight rows to load, so nothing is requested before the previous
+      // kernel has finished.
+      griddep_wait();
+      const uint64_t pol_b = policy_evict_last();
+      int it = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        int mt, nt;
+        tile_coords(t, m_tiles, n_tiles, mt, nt);
+        const int g = group_of(mt);
+        if (g < 0 || g >= G) continue;
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (uint32_t(it) / kStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteProducerEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + size_t(s) * kStageBytes;
+          mbar_arrive_expect_tx(&full[s], kStageBytes + kStageAs);
+          tma_load_2d(sa, &tmA, &full[s], kb * BK, mt * BM);
+          tma_load_2d_hint(sa + kStageA, &tmB, &full[s], kb * BK, g * N + nt * BN, pol_b);
+          tma_load_2d(as_stage + s * BM, &tmAs, &full[s], mt * BM, kb);
+        }
+      }
+      if (!ok) {
+        const int first = it > kStages ? it - kStages : 0;
+        for (int j = first; j < it; ++j) mbar_wait(&full[j % kStages], (uint32_t(j) / kStages) & 1u, nullptr);
+      }
+    } else if (lane == 0) {
       // Items are this CTA's (tile, K block) pairs in order.
       const int nkb = kb_end - kb_begin;
       const int my_tiles = cluster_id < num_tiles ? (num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0;
@@ -231,6 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
       for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        if (row_group != nullptr) {
+          int mt, nt;
+          tile_coords(t, m_tiles, n_tiles, mt, nt);
+          const int g = group_of(mt);
+          if (g < 0 || g >= G) continue;
+        }
         for (int kb = kb_begin; kb < kb_end; ++kb, ++it, ++acc_it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
@@ -271,6 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
       int mt, nt;
       tile_coords(t, m_tiles, n_tiles, mt, nt);
+      const int g = group_of(mt);
+      if (g < 0 || g >= G) {
+        // Padding tile, or a group index past the weights: skipped by every
+        // role; the latter is also reported in the error word.
+        if (g >= G && threadIdx.x == 64) atomicCAS(err, 0, kDevErrW8A8 | kSiteBadGroup);
+        continue;
+      }
       last_mt = mt;
       last_nt = nt;
       const int m = mt * BM + row_in_tile;
@@ -279,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kColsPerThread; ++j) acc[j] = 0.f;
       // Weight scales of this tile: lane j holds Bs[nt, kb0 + j] for a window
       // of 32 K blocks, handed out by shuffle (one load per 32 blocks).
-      const float* bs_row = Bs + size_t(nt) * kblocks;
+      const float* bs_row = Bs + (size_t(g) * n_tiles + nt) * kblocks;
       float bs_win = 0.f;
       for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
         const int rel = kb - kb_begin;
@@ -383,7 +438,7 @@ cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStre
   const int tiles = m_tiles * n_tiles;
   const int kblocks = p.K / BK;
   int split = 1;
-  if (tiles * 2 <= dev.num_sms) {
+  if (tiles * 2 <= dev.num_sms && p.row_group == nullptr) {
     for (int s = kMaxSplitK; s >= 2; s >>= 1) {
       if (tiles * s <= dev.num_sms && kblocks >= 2 * s) {
         split = s;
@@ -408,14 +463,16 @@ cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStre
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, w8a8_kernel<OutT>, p.tmA, p.tmB, p.tmAs, p.Bs, static_cast<OutT*>(p.C), p.ldc,
-                            p.M, p.N, p.K, split, p.err);
+                            p.M, p.N, p.K, split, p.row_group, p.groups, p.err);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
-  // Enough 256x256 tiles to keep most CTA pairs busy: the pair kernel.
-  if (p.M > kW8A8TileM && 2 * w8a8_pair_tiles(p.M, p.N) >= dev.num_sms / 2) return launch_gemm_w8a8_pair(p, dev, stream);
+  // Enough 256x256 tiles to keep most CTA pairs busy: the pair kernel
+  // (ungrouped problems only).
+  if (p.row_group == nullptr && p.M > kW8A8TileM && 2 * w8a8_pair_tiles(p.M, p.N) >= dev.num_sms / 2)
+    return launch_gemm_w8a8_pair(p, dev, stream);
   return p.out_f32 ? launch_single<float>(p, dev, stream) : launch_single<__nv_bfloat16>(p, dev, stream);
 }
 

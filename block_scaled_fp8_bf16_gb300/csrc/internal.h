@@ -27,6 +27,7 @@ enum WaitSite : int {
   kSiteDrain = 8,
   kSiteReduceEmpty = 9,
   kSiteReduceFull = 10,
+  kSiteBadGroup = 11,   // not a wait: a grouped tile named a group past the weights
 };
 
 struct DeviceInfo {
@@ -83,6 +84,8 @@ struct GemmW8A8Args {
   int M, N, K;
   bool pdl;           // launch with programmatic stream serialisation
   bool out_f32;       // C is float32 (ldc in float32 elements), else bf16
+  const int* row_group = nullptr;   // grouped form: group of each row (device), else nullptr
+  int groups = 1;                   // G: the weights are [G*N, K], their scales [G][N/128][K/128]
   int* err;
 };
 constexpr int kW8A8TileM = 128;

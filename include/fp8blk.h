@@ -173,6 +173,38 @@ FP8BLK_API fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda,
                                uint32_t flags, fp8blk_stream_t stream);
 
 /*
+ * Grouped (mixture-of-experts) W8A8 GEMM: the same block-scaled product as
+ * fp8blk_gemm_w8a8, but row m of A is multiplied by the weights of group
+ * row_group[m] (one expert per row).  The rows of each group are stored
+ * contiguously in whole 128-row tiles (the token rows routed to one expert,
+ * padded to a multiple of 128), so the group is constant over every aligned
+ * 128-row block of A and C; a block whose group is negative is padding and
+ * is skipped (its C rows are not written).
+ *
+ *  a_e4m3, a_scales, lda, lds   as fp8blk_gemm_w8a8, for all M rows.
+ *  b_e4m3     [G][N][K] e4m3: group g's weights are rows g*N .. g*N+N-1 of a
+ *             [G*N, K] matrix with row pitch ldb bytes.
+ *  b_scales   [G][N/128][K/128] float32, packed.
+ *  row_group  device int32 [M]; row_group[m] in [0, G) or negative (padding),
+ *             constant within each aligned 128-row block.  A block naming a
+ *             group >= G is skipped and reported through the device error word.
+ *  c_bf16     [M, N] out as fp8blk_gemm_w8a8 (FP8BLK_FLAG_OUT_F32 allowed).
+ *  M % 128 == 0, N % 128 == 0, K % 128 == 0, G >= 1.  K == 0 zero-fills all
+ *  M rows of C.
+ *  flags      FP8BLK_FLAG_PDL (the weights are then read only after the
+ *             previous kernel, since row_group decides which) and
+ *             FP8BLK_FLAG_OUT_F32.
+ */
+FP8BLK_API fp8blk_status fp8blk_gemm_w8a8_grouped(const void* a_e4m3, int64_t lda,
+                               const float* a_scales, int64_t lds,
+                               const void* b_e4m3, int64_t ldb,
+                               const float* b_scales,
+                               const int32_t* row_group, int64_t G,
+                               void* c_bf16, int64_t ldc,
+                               int64_t M, int64_t N, int64_t K,
+                               uint32_t flags, fp8blk_stream_t stream);
+
+/*
  * W8A16 GEMM: bf16 activations, e4m3 weights decoded to bf16 in registers by
  * integer operations, bf16 tensor-core products with FP32 accumulation
  * ("FP8 / NVFP4 weight-only inference on the RTX 3090 loses nothing",

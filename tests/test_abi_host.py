@@ -170,3 +170,19 @@ def test_wait_timeout_diag_argument_errors(fp8blk):
     L = fp8blk._L()
     for bad in (0, 999, 100_000_001, -5):
         assert L.fp8blk_debug_wait_timeout(bad, None) == 1   # FP8BLK_ERR_INVALID_ARG, no device work
+
+
+def test_grouped_argument_errors(fp8blk):
+    L = fp8blk._L()
+    P = ctypes.c_void_p(16 * 1024)   # a fake, 16-byte aligned device address: never dereferenced on these paths
+
+    def g(M=256, N=256, K=512, G=2, rg=P, lda=512, lds=256, ldb=512, ldc=256, flags=0):
+        return L.fp8blk_gemm_w8a8_grouped(P, lda, P, lds, P, ldb, P, rg, G, P, ldc, M, N, K, flags, None)
+
+    assert g(G=0) == 1                 # at least one group
+    assert g(M=200) == 2               # M % 128 for grouped rows
+    assert g(N=200) == 2
+    assert g(rg=None) == 1             # the row groups are required
+    assert g(rg=ctypes.c_void_p(16 * 1024 + 2)) == 3   # int32 alignment
+    assert g(flags=4) == 1
+    assert g(M=0) == 0 and g(N=0) == 0  # no-ops, no device needed
