@@ -387,63 +387,42 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
 
   __syncwarp();   // single-lane roles rejoin their warp before the aligned barriers below
   if (split > 1) {
-    // Rank 0 sums the ranks' partial tiles, in rank order, from distributed
-    // shared memory.
+    // Every rank publishes its partial tile [TM tokens][BN rows] in its own
+    // shared memory; then rank r sums the token rows
+    // [r * TM / split, (r + 1) * TM / split) over all ranks, in rank order,
+    // and stores them.  Consecutive threads take consecutive weight rows, so
+    // the remote reads and the stores are coalesced and every rank shares
+    // the reduction.
     const bool epi = warp >= 2 + Q::kDecWarps;
-    if constexpr (TM < 128) {
-      // Each thread's columns are stored contiguously, so the remote reads
-      // are 16-byte vectors, four in flight.
-      float4* red = reinterpret_cast<float4*>(smem);   // [BN rows][TM / 4] float4, reuses the stages
-      if (epi && rank != 0) {
+    float* red = reinterpret_cast<float*>(smem);   // [TM][BN] floats, reuses the stages
+    if (epi) {
 #pragma unroll
-        for (int j4 = 0; j4 < EC / 4; ++j4)
-          red[row * (TM / 4) + col0 / 4 + j4] =
-              make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
-      }
-      cluster_sync();
-      if (epi && rank == 0) {
-        for (int r = 1; r < split; ++r) {
-          const uint32_t base =
-              map_shared_rank(smem_u32(red), uint32_t(r)) + uint32_t((row * (TM / 4) + col0 / 4) * 16);
+      for (int j = 0; j < EC; ++j) red[(col0 + j) * BN + row] = acc[j];
+    }
+    cluster_sync();
+    if (epi && !*abort_flag) {
+      const int et = (warp - 2 - Q::kDecWarps) * 32 + lane;   // 0 .. 32 * kEpiWarps - 1
+      constexpr int kTStep = 32 * Q::kEpiWarps / BN;          // token rows handled per pass
+      static_assert(32 * Q::kEpiWarps % BN == 0, "whole token rows per pass");
+      const int r_row = et % BN;
+      const int t_end = (TM * (rank + 1)) / split;
+      const int m0 = last_mt * TM;
+      const int n0 = last_nt * BN;
+      uint32_t base[kMaxSplitK];
 #pragma unroll
-          for (int g = 0; g < EC / 16; ++g) {
-            float4 v[4];
+      for (int r = 0; r < kMaxSplitK; ++r)
+        if (r < split) base[r] = map_shared_rank(smem_u32(red), uint32_t(r)) + uint32_t(r_row) * 4u;
+      for (int t = (TM * rank) / split + et / BN; t < t_end && m0 + t < M; t += kTStep) {
+        const uint32_t off = uint32_t(t * BN) * 4u;
+        float v[kMaxSplitK];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = ld_dsmem_f4(base + uint32_t((4 * g + q) * 16));
+        for (int r = 0; r < kMaxSplitK; ++r)
+          if (r < split) v[r] = ld_dsmem_f32(base[r] + off);
+        float sum = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int j = 16 * g + 4 * q;
-              acc[j] += v[q].x;
-              acc[j + 1] += v[q].y;
-              acc[j + 2] += v[q].z;
-              acc[j + 3] += v[q].w;
-            }
-          }
-        }
-        if (!*abort_flag) store_col<EC>(C, ldc, M, last_mt * TM + col0, last_nt * BN + row, acc);
-      }
-    } else {
-      // Widest tile (rarely split): scalar remote reads keep register use low.
-      float* red = reinterpret_cast<float*>(smem);   // [TM][BN] floats, reuses the stages
-      if (epi && rank != 0) {
-#pragma unroll
-        for (int j = 0; j < EC; ++j) red[(col0 + j) * BN + row] = acc[j];
-      }
-      cluster_sync();
-      if (epi && rank == 0) {
-        for (int r = 1; r < split; ++r) {
-          const uint32_t base = map_shared_rank(smem_u32(red), uint32_t(r));
-#pragma unroll
-          for (int j = 0; j < EC; ++j) {
-            float v;
-            asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                         : "=f"(v)
-                         : "r"(base + uint32_t(((col0 + j) * BN + row) * 4))
-                         : "memory");
-            acc[j] += v;
-          }
-        }
-        if (!*abort_flag) store_col<EC>(C, ldc, M, last_mt * TM + col0, last_nt * BN + row, acc);
+        for (int r = 0; r < kMaxSplitK; ++r)
+          if (r < split) sum += v[r];
+        C[size_t(m0 + t) * ldc + n0 + r_row] = to_out(sum, C);
       }
     }
     cluster_sync();
