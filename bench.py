@@ -485,6 +485,11 @@ def sweep(out_path, kinds=None):
                                             fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"],
                                                                     flags=f)) for s in sets]
             record("w8a8_linear" + tag, M, N, K, graph_time(calls2), 2.0 * M * N * K, byt + 2 * M * K, fp8_peak)
+            if M <= fp8blk.LINEAR_FUSED_MAX_M:
+                calls3 = [lambda s=s, f=flags: fp8blk.fp8blk_linear_w8a8(s["x"], s["b"], s["bs"], s["c"], flags=f)
+                          for s in sets]
+                record("w8a8_linear_fused" + tag, M, N, K, graph_time(calls3), 2.0 * M * N * K,
+                       byt + 2 * M * K - M * K - (K // 128) * M * 4, fp8_peak)
         qcalls = [lambda s=s: fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"]) for s in sets]
         record("quant_act", M, 0, K, graph_time(qcalls), 0.0, 3 * M * K + (K // 128) * M * 4, fp8_peak)
         del sets

@@ -25,6 +25,9 @@ SCALE_UE8M0_32x32 = 1
 FLAG_PDL = 1
 FLAG_OUT_F32 = 2
 
+# Largest token count fp8blk_linear_w8a8 takes (quantisation fused into the GEMM).
+LINEAR_FUSED_MAX_M = 32
+
 STATUS_NAMES = {
     0: "FP8BLK_OK",
     1: "FP8BLK_ERR_INVALID_ARG",
@@ -45,6 +48,7 @@ _U32 = ctypes.c_uint32
 EXPORTS = {
     "fp8blk_quant_act": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
     "fp8blk_gemm_w8a8": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _U32, _P]),
+    "fp8blk_linear_w8a8": (_I32, [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_gemm_w8a8_grouped": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _I64, _U32,
                                          _P]),
     "fp8blk_gemm_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _U32, _P]),
@@ -161,6 +165,18 @@ def fp8blk_gemm_w8a8(a, a_scales, b, b_scales, c, stream=None, flags=0):
     N = b.shape[0]
     _check(_L().fp8blk_gemm_w8a8(_ptr(a), _ld(a), _ptr(a_scales), _ld(a_scales), _ptr(b), _ld(b), _ptr(b_scales),
                                 _ptr(c), _ld(c), M, N, K, _out_flags(c, flags), _stream(stream)), "fp8blk_gemm_w8a8")
+
+
+def fp8blk_linear_w8a8(x, b, b_scales, c, stream=None, flags=0):
+    """Decode-size (M <= 32) W8A8 linear in one launch: x [M, K] bf16 is quantised
+    per token per 128 inside the GEMM kernel; C as fp8blk_gemm_w8a8."""
+    import torch
+    _expect(x, (torch.bfloat16,), "x")
+    b = _bytes_tensor(b)
+    M, K = x.shape
+    N = b.shape[0]
+    _check(_L().fp8blk_linear_w8a8(_ptr(x), _ld(x), _ptr(b), _ld(b), _ptr(b_scales), _ptr(c), _ld(c), M, N, K,
+                                  _out_flags(c, flags), _stream(stream)), "fp8blk_linear_w8a8")
 
 
 def fp8blk_gemm_w8a8_grouped(a, a_scales, b, b_scales, row_group, c, stream=None, flags=0):
@@ -298,10 +314,17 @@ def gemv_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None, fla
     return out
 
 
-def linear_w8a8(x, b, b_scales, out=None, stream=None):
-    """bf16 x -> per-token quantisation -> W8A8 GEMM (two launches)."""
+def linear_w8a8(x, b, b_scales, out=None, stream=None, flags=0, out_dtype=None):
+    """bf16 x -> per-token quantisation -> W8A8 GEMM: one fused launch for
+    M <= 32, else quant_act + gemm_w8a8 (two launches)."""
+    import torch
+    if x.shape[0] <= LINEAR_FUSED_MAX_M:
+        if out is None:
+            out = torch.empty((x.shape[0], b.shape[0]), dtype=out_dtype or torch.bfloat16, device=x.device)
+        fp8blk_linear_w8a8(x, b, b_scales, out, stream, flags)
+        return out
     a, s = quant_act(x, stream)
-    return gemm_w8a8(a, s, b, b_scales, out, stream)
+    return gemm_w8a8(a, s, b, b_scales, out, stream, flags, out_dtype)
 
 
 def validate_weights(b, b_scales, fmt=SCALE_F32_128x128, stream=None):

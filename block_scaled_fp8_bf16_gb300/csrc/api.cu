@@ -233,6 +233,7 @@ fp8blk_status run_w8a8(const void* a_e4m3, int64_t lda, const float* a_scales, i
   if (K == 0) return zero_output(c_bf16, ldc, M, N, f32 ? 4 : 2, s);
   const int64_t b_rows = G > 0 ? G * N : N;
   GemmW8A8Args p;
+  std::memset(&p.tmX, 0, sizeof(p.tmX));     // read only by the fused form
   st = make_map(p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_e4m3, uint64_t(K), uint64_t(M), uint64_t(lda), 128,
                 kW8A8TileM);
   if (st != FP8BLK_OK) return st;
@@ -295,6 +296,50 @@ fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda, const float* a_s
                                int64_t M, int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
   return run_w8a8(a_e4m3, lda, a_scales, lds, b_e4m3, ldb, b_scales, nullptr, 0, c_bf16, ldc, M, N, K, flags,
                   stream);
+}
+
+fp8blk_status fp8blk_linear_w8a8(const void* x_bf16, int64_t ldx, const void* b_e4m3, int64_t ldb,
+                                 const float* b_scales, void* c_bf16, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                 uint32_t flags, fp8blk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || (flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0 || M > kW8A8FusedMaxM) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
+  if (N > kIntMax || K > kIntMax) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return FP8BLK_OK;
+  if (!c_bf16) return FP8BLK_ERR_INVALID_ARG;
+  if (K > 0 && (!x_bf16 || !b_e4m3 || !b_scales)) return FP8BLK_ERR_INVALID_ARG;
+  if (ldx < K || ldb < K || ldc < N) return FP8BLK_ERR_INVALID_ARG;
+  if ((x_bf16 && !aligned16(x_bf16)) || (b_e4m3 && !aligned16(b_e4m3)) || (b_scales && !aligned16(b_scales)) ||
+      !aligned16(c_bf16))
+    return FP8BLK_ERR_MISALIGNED;
+  const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
+  if ((ldx * 2) % 16 != 0 || ldb % 16 != 0 || (ldc * (f32 ? 4 : 2)) % 16 != 0) return FP8BLK_ERR_MISALIGNED;
+  DeviceInfo dev;
+  fp8blk_status st = device_info(dev);
+  if (st != FP8BLK_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(c_bf16, ldc, M, N, f32 ? 4 : 2, s);
+  GemmW8A8Args p;
+  std::memset(&p.tmA, 0, sizeof(p.tmA));     // not read by the fused form
+  std::memset(&p.tmAs, 0, sizeof(p.tmAs));
+  std::memset(&p.tmAsG, 0, sizeof(p.tmAsG));
+  std::memset(&p.tmC, 0, sizeof(p.tmC));
+  st = make_map(p.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x_bf16, uint64_t(K), uint64_t(M), uint64_t(ldx) * 2, 64,
+                uint32_t(kW8A8FusedMaxM));
+  if (st != FP8BLK_OK) return st;
+  st = make_map(p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_e4m3, uint64_t(K), uint64_t(N), uint64_t(ldb), 128,
+                kW8A8TileN);
+  if (st != FP8BLK_OK) return st;
+  p.Bs = b_scales;
+  p.C = c_bf16;
+  p.ldc = ldc;
+  p.M = int(M);
+  p.N = int(N);
+  p.K = int(K);
+  p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
+  p.out_f32 = f32;
+  p.fused = true;
+  p.err = dev.err_word;
+  return cuda_status(launch_gemm_w8a8(p, dev, s));
 }
 
 fp8blk_status fp8blk_gemm_w8a8_grouped(const void* a_e4m3, int64_t lda, const float* a_scales, int64_t lds,

@@ -49,6 +49,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace fp8blk {
 namespace {
@@ -62,21 +63,40 @@ constexpr int kStageB = BN * BK;
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kStageAs = BM * 4;          // fp32 activation scales of the tile's rows for one K block
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kColsPerThread = BN / 2;   // two epilogue warps share a TMEM lane quarter
 constexpr int kAccBufs = 4;              // FP32 partials in flight in TMEM
 constexpr uint32_t kTmemCols = kAccBufs * BN;
 constexpr uint32_t kIdesc = make_idesc(0 /* e4m3 */, BM, BN);
 constexpr int kGroupM = 8;
 constexpr int kBarrierBytes = 512;
-constexpr size_t kSmemBytes = size_t(kStages) * (kStageBytes + kStageAs) + kBarrierBytes + 1024;
 
 static_assert(BK == 128, "one MMA K block must be exactly one scale block");
 static_assert(kTmemCols <= 512, "TMEM budget");
 static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 N for M = 128");
 static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "128B-swizzle atoms need 1024-B alignment");
 static_assert(2 * kStageBytes >= BM * BN * 4, "split-K reduction buffer reuses two stages");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+// Configuration of the kernel.  FUSED quantises the activations itself: the
+// producer loads bf16 token rows (at most kFusedMaxM, one 32-row tile) and
+// the quantiser warps turn each 128-wide K block into e4m3 codes and a scale
+// per row, with the arithmetic of the stand-alone quantiser (quant.cuh), into
+// the stage's A tile and scale slot (two quantiser warps).
+// Otherwise A and As arrive by TMA.
+constexpr int kFusedMaxM = kW8A8FusedMaxM;
+template <bool FUSED>
+struct W8A8Cfg {
+  static constexpr int kStages = FUSED ? 5 : fp8blk::kStages;
+  static constexpr int kQuantWarps = FUSED ? 2 : 0;   // 12 warps: 168 registers per thread
+  static constexpr int kThreads = 64 + (kEpiWarps + kQuantWarps) * 32;
+  static constexpr int kStageX = FUSED ? kFusedMaxM * BK * 2 : 0;   // bf16 [32][128] as two 64-column boxes
+  static constexpr size_t kAsOff = size_t(kStages) * kStageBytes;
+  static constexpr size_t kXOff = (kAsOff + size_t(kStages) * kStageAs + 1023) / 1024 * 1024;
+  static constexpr size_t kBarOff = kXOff + size_t(kStages) * kStageX;
+  static constexpr size_t kSmemBytes = kBarOff + kBarrierBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert((3 * kStages + 2 * kAccBufs + 1) * 8 + 8 <= kBarrierBytes, "barrier area");
+  static_assert(kFusedMaxM % (4 * (FUSED ? kQuantWarps : 1)) == 0, "whole passes of four rows per quantiser warp");
+};
+static_assert(W8A8Cfg<false>::kBarOff == size_t(kStages) * (kStageBytes + kStageAs), "unfused layout unchanged");
 
 __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mt, int& nt) {
   const int per_group = kGroupM * n_tiles;
@@ -113,22 +133,30 @@ __device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* acc
 }
 
 // OutT: __nv_bfloat16 (rounded to nearest even) or float (the accumulator as is).
-template <class OutT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <class OutT, bool FUSED>
+__global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
     w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmAs, const float* __restrict__ Bs,
+                const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmX,
+                const float* __restrict__ Bs,
                 OutT* __restrict__ C, int64_t ldc, int M, int N, int K, int split,
                 const int* __restrict__ row_group, int G, int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  float* as_stage = reinterpret_cast<float*>(smem + size_t(kStages) * kStageBytes);   // [kStages][BM]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * (kStageBytes + kStageAs));
+  using Q = W8A8Cfg<FUSED>;
+  constexpr int kStages = Q::kStages;
+  float* as_stage = reinterpret_cast<float*>(smem + Q::kAsOff);   // [kStages][BM]
+  uint8_t* x_stage = smem + Q::kXOff;                            // [kStages][kStageX] (FUSED)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Q::kBarOff);
   uint64_t* empty = full + kStages;
   uint64_t* dfull = empty + kStages;
   uint64_t* dempty = dfull + kAccBufs;
   uint64_t* drain = dempty + kAccBufs;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  // FUSED: the weight tile and the bf16 token rows of a stage complete on
+  // xfull[s]; full[s] then completes when the quantiser warps have written
+  // the codes and scales.
+  uint64_t* xfull = drain + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(xfull + kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   griddep_launch_dependents();   // the next kernel may start its prologue; it gets an SM when this CTA leaves
@@ -149,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], FUSED ? Q::kQuantWarps : 1);
+      mbar_init(&xfull[s], 1);
       mbar_init(&empty[s], 1 + kEpiWarps);   // MMA done with A/B, epilogue done with the scales
     }
     for (int d = 0; d < kAccBufs; ++d) {
@@ -165,9 +194,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
+    if constexpr (FUSED) {
+      tma_prefetch_desc(&tmX);
+    } else {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmAs);
+    }
     tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmAs);
   }
   tc_fence_before();
   __syncthreads();
@@ -184,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && row_group != nullptr) {
+    if (lane == 0 && !FUSED && row_group != nullptr) {
       // Grouped: the tile's group (an activation-side input) decides which
       // weight rows to load, so nothing is requested before the previous
       // kernel has finished.
@@ -227,21 +260,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Under programmatic dependent launch the weight tiles of the first
       // stages are requested before the previous kernel has finished; the
       // activations and their scales only after it.
+      // The barrier the stage's copies complete on, and their bytes.
+      uint64_t* const cbar = FUSED ? xfull : full;
+      constexpr uint32_t kTx = FUSED ? uint32_t(kStageB + Q::kStageX) : uint32_t(kStageBytes + kStageAs);
+      // Activation-side copies of item it into stage s: A + As, or the bf16
+      // token rows (two 64-column boxes) that the quantiser warps consume.
+      auto load_act = [&](int s, int mt, int kb) {
+        if constexpr (FUSED) {
+          tma_load_2d(x_stage + size_t(s) * Q::kStageX, &tmX, &xfull[s], kb * BK, 0);
+          tma_load_2d(x_stage + size_t(s) * Q::kStageX + Q::kStageX / 2, &tmX, &xfull[s], kb * BK + 64, 0);
+        } else {
+          tma_load_2d(smem + size_t(s) * kStageBytes, &tmA, &full[s], kb * BK, mt * BM);
+          tma_load_2d(as_stage + s * BM, &tmAs, &full[s], mt * BM, kb);
+        }
+      };
       const int pre = n_items < kStages ? n_items : kStages;
       for (int it = 0; it < pre; ++it) {
         int mt, nt;
         tile_coords(cluster_id + (it / nkb) * num_clusters, m_tiles, n_tiles, mt, nt);
         const int kb = kb_begin + it % nkb;
-        mbar_arrive_expect_tx(&full[it], kStageBytes + kStageAs);
-        tma_load_2d_hint(smem + size_t(it) * kStageBytes + kStageA, &tmB, &full[it], kb * BK, nt * BN, pol_b);
+        mbar_arrive_expect_tx(&cbar[it], kTx);
+        tma_load_2d_hint(smem + size_t(it) * kStageBytes + kStageA, &tmB, &cbar[it], kb * BK, nt * BN, pol_b);
       }
       griddep_wait();
       for (int it = 0; it < pre; ++it) {
         int mt, nt;
         tile_coords(cluster_id + (it / nkb) * num_clusters, m_tiles, n_tiles, mt, nt);
-        const int kb = kb_begin + it % nkb;
-        tma_load_2d(smem + size_t(it) * kStageBytes, &tmA, &full[it], kb * BK, mt * BM);
-        tma_load_2d(as_stage + it * BM, &tmAs, &full[it], mt * BM, kb);
+        load_act(it, mt, kb_begin + it % nkb);
       }
       int it = pre;
       for (; it < n_items; ++it) {
@@ -254,17 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mt, nt;
         tile_coords(cluster_id + (it / nkb) * num_clusters, m_tiles, n_tiles, mt, nt);
         const int kb = kb_begin + it % nkb;
-        uint8_t* sa = smem + size_t(s) * kStageBytes;
-        uint8_t* sb = sa + kStageA;
-        mbar_arrive_expect_tx(&full[s], kStageBytes + kStageAs);
-        tma_load_2d(sa, &tmA, &full[s], kb * BK, mt * BM);
-        tma_load_2d_hint(sb, &tmB, &full[s], kb * BK, nt * BN, pol_b);
-        tma_load_2d(as_stage + s * BM, &tmAs, &full[s], mt * BM, kb);
+        mbar_arrive_expect_tx(&cbar[s], kTx);
+        load_act(s, mt, kb);
+        tma_load_2d_hint(smem + size_t(s) * kStageBytes + kStageA, &tmB, &cbar[s], kb * BK, nt * BN, pol_b);
       }
       if (it < n_items) {
         // Let every copy this thread issued land before the CTA can exit.
         const int first = it > kStages ? it - kStages : 0;
-        for (int j = first; j < it; ++j) mbar_wait(&full[j % kStages], (uint32_t(j) / kStages) & 1u, nullptr);
+        for (int j = first; j < it; ++j) mbar_wait(&cbar[j % kStages], (uint32_t(j) / kStages) & 1u, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -311,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ promotion + epilogue
     griddep_wait();        // the output may still be read or written by the previous kernel
     uint32_t it = 0;       // stage counter, in step with the producer and the MMA issuer
@@ -362,20 +404,158 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t p[kColsPerThread];
         const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(d * BN + half * kColsPerThread);
-        tmem_ld_x32(taddr, p);
-        tmem_ld_x32(taddr + 32, p + 32);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&dempty[d]);
         const float sc = sa * sb;
+        if constexpr (FUSED) {
+          // 128 registers per thread in this configuration: one 32-column
+          // load at a time.
 #pragma unroll
-        for (int j = 0; j < kColsPerThread; ++j) acc[j] = fmaf(__uint_as_float(p[j]), sc, acc[j]);
+          for (int h = 0; h < kColsPerThread / 32; ++h) {
+            uint32_t p[32];
+            tmem_ld_x32(taddr + uint32_t(32 * h), p);
+            tmem_ld_wait();
+            if (h + 1 == kColsPerThread / 32) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&dempty[d]);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 * h + j] = fmaf(__uint_as_float(p[j]), sc, acc[32 * h + j]);
+          }
+        } else {
+          uint32_t p[kColsPerThread];
+          tmem_ld_x32(taddr, p);
+          tmem_ld_x32(taddr + 32, p + 32);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&dempty[d]);
+#pragma unroll
+          for (int j = 0; j < kColsPerThread; ++j) acc[j] = fmaf(__uint_as_float(p[j]), sc, acc[j]);
+        }
       }
       if (ok && split == 1 && row_ok) {
         store_row64(C + size_t(m) * ldc + size_t(nt) * BN + half * kColsPerThread, acc);
+      }
+    }
+  } else if constexpr (FUSED) {
+    // ------------------------------------------------------------ activation quantisers
+    // Eight lanes share a token row (16 columns each, the row's amax from
+    // three xor shuffles inside the group), a warp covers four rows per
+    // pass, and the warps interleave: pass j of warp q takes rows
+    // 8j + 4q .. 8j + 4q + 3, so both warps work from the fifth row on.  Codes go to the 128-byte-swizzled A tile the MMA
+    // reads, one 16-byte chunk per lane and row.
+    const int qw = warp - 2 - kEpiWarps;
+    const int sub = lane & 7;              // 16-column slice of the row
+    const int rg = lane >> 3;              // row within the pass
+    constexpr int kPasses = kFusedMaxM / (4 * Q::kQuantWarps);
+    constexpr int kNarrowM = 8;            // up to this many rows: one warp per row
+    static_assert(kPasses % 2 == 0, "passes run in pairs");
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&xfull[s], ph, abort_flag))) {
+          raise_error(err, abort_flag, kSiteDecodeFull);
+          ok = false;
+          break;
+        }
+        // Columns 16 sub .. 16 sub + 15 are chunks 2 (sub & 3), +1 of box sub / 4.
+        const uint8_t* xs = x_stage + size_t(s) * Q::kStageX + (sub >> 2) * (Q::kStageX / 2);
+        uint8_t* a_tile = smem + size_t(s) * kStageBytes;
+        if (M <= kNarrowM) {
+          // Few rows: a whole warp per row (four columns per lane, amax from
+          // five xor shuffles), warp q taking rows q, q + 2, ..., two at a
+          // time as independent chains.
+#pragma unroll
+          for (int i0 = 0; i0 < kNarrowM / Q::kQuantWarps; i0 += 2) {
+            if (qw + Q::kQuantWarps * i0 >= M) break;   // warp-uniform
+            float f[2][4];
+            int r[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              r[u] = qw + Q::kQuantWarps * (i0 + u);
+              const uint2 v = *reinterpret_cast<const uint2*>(
+                  x_stage + size_t(s) * Q::kStageX + (lane >> 4) * (Q::kStageX / 2) + r[u] * 128 +
+                  ((((lane & 15) >> 1) ^ (r[u] & 7)) << 4) + (lane & 1) * 8);
+              f[u][0] = __uint_as_float(v.x << 16);
+              f[u][1] = __uint_as_float(v.x & 0xFFFF0000u);
+              f[u][2] = __uint_as_float(v.y << 16);
+              f[u][3] = __uint_as_float(v.y & 0xFFFF0000u);
+            }
+            float amax[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              amax[u] = fmaxf(fmaxf(fabsf(f[u][0]), fabsf(f[u][1])), fmaxf(fabsf(f[u][2]), fabsf(f[u][3])));
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+              amax[0] = fmaxf(amax[0], __shfl_xor_sync(0xffffffffu, amax[0], o));
+              amax[1] = fmaxf(amax[1], __shfl_xor_sync(0xffffffffu, amax[1], o));
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const float sc = group_scale(amax[u]);
+              const Divisor dv = make_divisor(sc);
+              const uint32_t codes =
+                  e4m3x4(quotient(f[u][0], dv), quotient(f[u][1], dv), quotient(f[u][2], dv), quotient(f[u][3], dv));
+              if (r[u] < M) {
+                *reinterpret_cast<uint32_t*>(a_tile + r[u] * 128 + (((lane >> 2) ^ (r[u] & 7)) << 4) + (lane & 3) * 4) =
+                    codes;
+                if (lane == 0) as_stage[s * BM + r[u]] = sc;
+              }
+            }
+          }
+        } else {
+        // Passes run two at a time as independent chains (loads, amax,
+        // scale, quotients), so one pass's latency hides the other's.
+#pragma unroll
+        for (int j0 = 0; j0 < kPasses; j0 += 2) {
+          if (4 * Q::kQuantWarps * j0 + 4 * qw >= M) break;   // warp-uniform
+          float f[2][16];
+          int r[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            r[u] = 4 * Q::kQuantWarps * (j0 + u) + 4 * qw + rg;
+            const int rr = r[u] < kFusedMaxM ? r[u] : kFusedMaxM - 1;
+            const int c0 = 2 * (sub & 3);
+            const uint4 v0 = *reinterpret_cast<const uint4*>(xs + rr * 128 + (((c0 + 0) ^ (rr & 7)) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(xs + rr * 128 + (((c0 + 1) ^ (rr & 7)) << 4));
+            bf16x8_to_f32(v0, f[u]);
+            bf16x8_to_f32(v1, f[u] + 8);
+          }
+          float amax[2] = {0.f, 0.f};
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax[u] = fmaxf(amax[u], fabsf(f[u][i]));
+#pragma unroll
+          for (int o = 4; o >= 1; o >>= 1) {
+            amax[0] = fmaxf(amax[0], __shfl_xor_sync(0xffffffffu, amax[0], o));
+            amax[1] = fmaxf(amax[1], __shfl_xor_sync(0xffffffffu, amax[1], o));
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float sc = group_scale(amax[u]);
+            const Divisor dv = make_divisor(sc);
+            uint4 codes;
+            codes.x = e4m3x4(quotient(f[u][0], dv), quotient(f[u][1], dv), quotient(f[u][2], dv), quotient(f[u][3], dv));
+            codes.y = e4m3x4(quotient(f[u][4], dv), quotient(f[u][5], dv), quotient(f[u][6], dv), quotient(f[u][7], dv));
+            codes.z =
+                e4m3x4(quotient(f[u][8], dv), quotient(f[u][9], dv), quotient(f[u][10], dv), quotient(f[u][11], dv));
+            codes.w =
+                e4m3x4(quotient(f[u][12], dv), quotient(f[u][13], dv), quotient(f[u][14], dv), quotient(f[u][15], dv));
+            if (r[u] < M) {
+              *reinterpret_cast<uint4*>(a_tile + r[u] * 128 + ((sub ^ (r[u] & 7)) << 4)) = codes;
+              if (sub == 0) as_stage[s * BM + r[u]] = sc;
+            }
+          }
+        }
+        }
+        fence_async_shared();   // the codes are read by the tensor cores (async proxy)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
       }
     }
   }
@@ -385,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One tile per cluster: sum the ranks' accumulators through distributed
     // shared memory, in rank order, into rank 0.  Every thread of every CTA
     // reaches both cluster barriers, also after an abort.
-    const bool epi = warp >= 2;
+    const bool epi = warp >= 2 && warp < 2 + kEpiWarps;
     const int m = last_mt * BM + row_in_tile;
     const bool row_ok = epi && m < M;
     float4* red = reinterpret_cast<float4*>(smem);   // [BN/4][BM] float4, reuses stages 0-1
@@ -422,14 +602,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <class OutT>
+template <class OutT, bool FUSED>
 cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  using Q = W8A8Cfg<FUSED>;
   static bool attr_done[64] = {};
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   if (device < 64 && !attr_done[device]) {
-    e = cudaFuncSetAttribute(w8a8_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    e = cudaFuncSetAttribute(w8a8_kernel<OutT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(Q::kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_done[device] = true;
   }
@@ -450,8 +632,8 @@ cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStre
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(clusters * split), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(Q::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Q::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -462,8 +644,8 @@ cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStre
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_kernel<OutT>, p.tmA, p.tmB, p.tmAs, p.Bs, static_cast<OutT*>(p.C), p.ldc,
-                            p.M, p.N, p.K, split, p.row_group, p.groups, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a8_kernel<OutT, FUSED>, p.tmA, p.tmB, p.tmAs, p.tmX, p.Bs,
+                            static_cast<OutT*>(p.C), p.ldc, p.M, p.N, p.K, split, p.row_group, p.groups, p.err);
 }
 
 }  // namespace
@@ -471,9 +653,13 @@ cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStre
 cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
   // Enough 256x256 tiles to keep most CTA pairs busy: the pair kernel
   // (ungrouped problems only).
+  if (p.fused) {
+    if (p.M > kFusedMaxM || p.row_group != nullptr) return cudaErrorInvalidValue;
+    return p.out_f32 ? launch_single<float, true>(p, dev, stream) : launch_single<__nv_bfloat16, true>(p, dev, stream);
+  }
   if (p.row_group == nullptr && p.M > kW8A8TileM && 2 * w8a8_pair_tiles(p.M, p.N) >= dev.num_sms / 2)
     return launch_gemm_w8a8_pair(p, dev, stream);
-  return p.out_f32 ? launch_single<float>(p, dev, stream) : launch_single<__nv_bfloat16>(p, dev, stream);
+  return p.out_f32 ? launch_single<float, false>(p, dev, stream) : launch_single<__nv_bfloat16, false>(p, dev, stream);
 }
 
 }  // namespace fp8blk

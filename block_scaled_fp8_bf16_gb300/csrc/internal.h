@@ -78,6 +78,7 @@ struct GemmW8A8Args {
   CUtensorMap tmAs;   // fp32 [K/128][lds] read as {M, K/128}, box {128, 1}, no swizzle
   CUtensorMap tmAsG;  // the same scales, box {128, 8}: eight K blocks per copy (pair kernel)
   CUtensorMap tmC;    // C [M, N] pitch ldc, box {128 bytes of N, 32 (M)}, 128B swizzle (pair kernel's stores)
+  CUtensorMap tmX;    // fused form: bf16 x [M, K] pitch ldx, box {64 (K), 32 (M)}, 128B swizzle
   const float* Bs;    // [N/128][K/128]
   void* C;            // bf16 [M, ldc]
   int64_t ldc;
@@ -86,9 +87,11 @@ struct GemmW8A8Args {
   bool out_f32;       // C is float32 (ldc in float32 elements), else bf16
   const int* row_group = nullptr;   // grouped form: group of each row (device), else nullptr
   int groups = 1;                   // G: the weights are [G*N, K], their scales [G][N/128][K/128]
+  bool fused = false;               // quantise bf16 x (tmX) in the kernel; M <= kW8A8FusedMaxM
   int* err;
 };
 constexpr int kW8A8TileM = 128;
+constexpr int kW8A8FusedMaxM = 32;   // token rows the activation-quantising form takes
 constexpr int kW8A8TileN = 128;
 constexpr int kMaxSplitK = 8;
 cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t s);

@@ -173,6 +173,31 @@ FP8BLK_API fp8blk_status fp8blk_gemm_w8a8(const void* a_e4m3, int64_t lda,
                                uint32_t flags, fp8blk_stream_t stream);
 
 /*
+ * Decode-size W8A8 linear layer in one launch: per-token 1x128 quantisation
+ * of x fused into the block-scaled GEMM ("Blockwise FP8 on Ada GPUs, part 2",
+ * "The starting point" counts the activation quantisation inside the layer's
+ * time).  The kernel's producer loads the bf16 rows of each 128-wide K block
+ * and quantiser warps compute the codes and scales in shared memory with the
+ * same arithmetic as fp8blk_quant_act, so the result is bit for bit the
+ * result of fp8blk_quant_act followed by fp8blk_gemm_w8a8 on the same shape,
+ * without the intermediate e4m3 tensor in HBM and without a second launch.
+ *
+ *  x_bf16    [M, K] bf16, row pitch ldx elements (ldx*2 % 16 == 0).
+ *  b_e4m3, ldb, b_scales, c_bf16, ldc, N, K, flags   as fp8blk_gemm_w8a8
+ *            (FP8BLK_FLAG_PDL, FP8BLK_FLAG_OUT_F32).
+ *  1 <= M <= 32 (larger M: FP8BLK_ERR_UNSUPPORTED_SHAPE; call
+ *  fp8blk_quant_act and fp8blk_gemm_w8a8 with caller-owned buffers, where the
+ *  quantisation pass runs once instead of once per weight tile).  M == 0 is
+ *  a no-op.
+ */
+FP8BLK_API fp8blk_status fp8blk_linear_w8a8(const void* x_bf16, int64_t ldx,
+                               const void* b_e4m3, int64_t ldb,
+                               const float* b_scales,
+                               void* c_bf16, int64_t ldc,
+                               int64_t M, int64_t N, int64_t K,
+                               uint32_t flags, fp8blk_stream_t stream);
+
+/*
  * Grouped (mixture-of-experts) W8A8 GEMM: the same block-scaled product as
  * fp8blk_gemm_w8a8, but row m of A is multiplied by the weights of group
  * row_group[m] (one expert per row).  The rows of each group are stored

@@ -186,3 +186,19 @@ def test_grouped_argument_errors(fp8blk):
     assert g(rg=ctypes.c_void_p(16 * 1024 + 2)) == 3   # int32 alignment
     assert g(flags=4) == 1
     assert g(M=0) == 0 and g(N=0) == 0  # no-ops, no device needed
+
+
+def test_fused_linear_argument_errors(fp8blk):
+    L = fp8blk._L()
+    P = ctypes.c_void_p(16 * 1024)
+
+    def f(M=16, N=256, K=512, ldx=512, ldb=512, ldc=256, flags=0, x=P):
+        return L.fp8blk_linear_w8a8(x, ldx, P, ldb, P, P, ldc, M, N, K, flags, None)
+
+    assert f(M=33) == 2                # more token rows than the fused form takes
+    assert f(N=200) == 2 and f(K=500) == 2
+    assert f(M=-1) == 1 and f(flags=4) == 1
+    assert f(ldx=256) == 1             # ldx < K
+    assert f(x=None) == 1
+    assert f(ldx=516) == 3             # bf16 rows of x must be 16-byte multiples
+    assert f(M=0) == 0                 # no-op, no device needed
