@@ -287,7 +287,19 @@ fp8blk_status fp8blk_quant_act(const void* x_bf16, int64_t M, int64_t K, int64_t
   DeviceInfo dev;
   fp8blk_status st = device_info(dev);
   if (st != FP8BLK_OK) return st;
-  QuantActArgs p{x_bf16, M, K, ldx, a_e4m3, lda, a_scales, lds};
+  QuantActArgs p;
+  st = make_map(p.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x_bf16, uint64_t(K), uint64_t(M), uint64_t(ldx) * 2, 128,
+                kQuantTileRows, false);
+  if (st != FP8BLK_OK) return st;
+  p.x = x_bf16;
+  p.ldx = ldx;
+  p.M = M;
+  p.K = K;
+  p.a = a_e4m3;
+  p.lda = lda;
+  p.scales = a_scales;
+  p.lds = lds;
+  p.err = dev.err_word;
   return cuda_status(launch_quant_act(p, dev, reinterpret_cast<cudaStream_t>(stream)));
 }
 

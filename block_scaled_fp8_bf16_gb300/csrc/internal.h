@@ -15,6 +15,7 @@ enum DeviceErr : int {
   kDevErrW8A8 = 0x100,
   kDevErrW8A16 = 0x200,
   kDevErrW8A16Decode = 0x300,
+  kDevErrQuant = 0x400,
 };
 enum WaitSite : int {
   kSiteProducerEmpty = 1,
@@ -40,13 +41,17 @@ struct DeviceInfo {
 
 // ------------------------------------------------------------------ quant
 struct QuantActArgs {
-  const void* x;
-  int64_t M, K, ldx;
+  CUtensorMap tmX;    // bf16 x [M, K] pitch ldx, box {128 (K), kQuantTileRows (M)}, no swizzle
+  const void* x;      // the same tensor, for the few-row kernel
+  int64_t ldx;
+  int64_t M, K;
   void* a;
   int64_t lda;
   float* scales;
   int64_t lds;
+  int* err;
 };
+constexpr int kQuantTileRows = 64;   // token rows per tile of the activation quantiser (the x box height)
 cudaError_t launch_quant_act(const QuantActArgs& p, const DeviceInfo& dev, cudaStream_t s);
 
 struct QuantWeightArgs {

@@ -26,11 +26,132 @@
 namespace fp8blk {
 namespace {
 
+// Activation quantiser, persistent and fed by TMA.  A tile is 64 token rows
+// of one 128-wide group (16 KB of bf16); tile t covers rows 64 (t / G) ..
+// and group t % G (G = K / 128).  One producer thread keeps kQStages tiles
+// in flight per CTA.  Eight warps consume a tile: warp w takes rows
+// 8w .. 8w + 7, four lanes per row and 32 bf16 per lane (four 8-column
+// chunks, 32 columns apart, so a row's lanes read consecutive bytes), so the per-group
+// work (the row's amax from two xor shuffles, the IEEE scale division and
+// the reciprocal behind the correctly rounded quotients, all with the
+// arithmetic of quant.cuh) is spread over 32 elements per lane.  Rows past M
+// arrive zero-filled and are not stored.
+constexpr int kQTileRows = kQuantTileRows;
+constexpr int64_t kQuantSmallM = 256;   // up to this many rows the register-fed kernel below runs
+constexpr int kQTileBytes = kQTileRows * 128 * 2;
+constexpr int kQStages = 6;
+constexpr int kQWarps = 8;
+constexpr int kQThreads = (kQWarps + 1) * 32;
+constexpr size_t kQSmemBytes = size_t(kQStages) * kQTileBytes + 2 * kQStages * 8 + 1024;
+
+__device__ __forceinline__ void quant_raise(int* err, volatile int* abort_flag, int site) {
+  *abort_flag = 1;
+  atomicCAS(err, 0, kDevErrQuant | site);
+}
+
+__global__ void __launch_bounds__(kQThreads) quant_act_kernel(const __grid_constant__ CUtensorMap tmX, int64_t M,
+                                                              int64_t K, uint8_t* __restrict__ a, int64_t lda,
+                                                              float* __restrict__ scales, int64_t lds,
+                                                              int* __restrict__ err) {
+  // A GEMM launched after this kernel with programmatic dependent launch may
+  // begin streaming its weights now; it waits for this grid before reading
+  // the codes and scales written here.
+  griddep_launch_dependents();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kQStages) * kQTileBytes);
+  uint64_t* empty = full + kQStages;
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t groups = K / 128;
+  const int64_t num_tiles = ((M + kQTileRows - 1) / kQTileRows) * groups;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kQWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == kQWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmX);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+        const int s = it % kQStages;
+        if (!mbar_wait(&empty[s], ((it / kQStages) & 1u) ^ 1u, abort_flag)) {
+          quant_raise(err, abort_flag, kSiteProducerEmpty);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kQTileBytes);
+        tma_load_2d(smem + size_t(s) * kQTileBytes, &tmX, &full[s], int32_t((t % groups) * 128),
+                    int32_t((t / groups) * kQTileRows));
+      }
+      if (!ok) {
+        const uint32_t first = it > uint32_t(kQStages) ? it - kQStages : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kQStages], (j / kQStages) & 1u, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ quantisers
+    const int sub = lane & 3;          // the row's 8-column chunks sub, sub + 4, sub + 8, sub + 12
+    const int row = 8 * warp + (lane >> 2);
+    uint32_t it = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      const int s = it % kQStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / kQStages) & 1u, abort_flag))) {
+        quant_raise(err, abort_flag, kSiteEpilogueFull);
+        break;
+      }
+      const int64_t g = t % groups;
+      const int64_t m0 = (t / groups) * kQTileRows;
+      // The four lanes of a row read 64 consecutive bytes per load.
+      const uint8_t* src = smem + size_t(s) * kQTileBytes + row * 256 + sub * 16;
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(src + j * 64);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);   // the rows are in registers: the stage can refill
+      float f[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bf16x8_to_f32(v[j], f + 8 * j);
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      const float sc = group_scale(amax);
+      const Divisor dv = make_divisor(sc);
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[i] = e4m3x4(quotient(f[4 * i], dv), quotient(f[4 * i + 1], dv), quotient(f[4 * i + 2], dv),
+                      quotient(f[4 * i + 3], dv));
+      const int64_t m = m0 + row;
+      if (m < M) {
+        uint8_t* dst = a + m * lda + g * 128 + sub * 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) *reinterpret_cast<uint2*>(dst + 32 * j) = make_uint2(w[2 * j], w[2 * j + 1]);
+        if (sub == 0) scales[g * lds + m] = sc;
+      }
+    }
+  }
+}
+
+// Few rows (M <= kQuantSmallM): no TMA ring, every warp loads its rows
+// straight into registers, which keeps the latency of a small call low.
 // Grid: x covers rows (each warp takes kQuantRows consecutive rows per
 // step), y covers pairs of 128-groups (lanes 0-15: group 2y, 16-31: 2y+1).
 constexpr int kQuantRows = 4;
 
-__global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
+__global__ void __launch_bounds__(256) quant_act_small_kernel(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K,
                                                         int64_t ldx, uint8_t* __restrict__ a, int64_t lda,
                                                         float* __restrict__ scales, int64_t lds) {
   // A GEMM launched after this kernel with programmatic dependent launch may
@@ -181,15 +302,32 @@ int grid_for(int64_t items, int per_block, int num_sms, int waves) {
 }  // namespace
 
 cudaError_t launch_quant_act(const QuantActArgs& p, const DeviceInfo& dev, cudaStream_t s) {
-  const int64_t pairs = (p.K / 128 + 1) / 2;
-  if (pairs > 65535) return cudaErrorInvalidValue;
-  const int64_t row_steps = (p.M + kQuantRows - 1) / kQuantRows;     // warps needed along M
-  int64_t gx = (row_steps + 7) / 8;
-  const int64_t cap = (int64_t(dev.num_sms) * 16 + pairs - 1) / pairs;  // about 16 CTAs per SM in total
-  if (gx > cap) gx = cap;
-  if (gx < 1) gx = 1;
-  quant_act_kernel<<<dim3(unsigned(gx), unsigned(pairs)), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(p.x), p.M, p.K, p.ldx,
-                                        static_cast<uint8_t*>(p.a), p.lda, p.scales, p.lds);
+  if (p.M <= kQuantSmallM) {
+    const int64_t pairs = (p.K / 128 + 1) / 2;
+    if (pairs > 65535) return cudaErrorInvalidValue;
+    const int64_t row_steps = (p.M + kQuantRows - 1) / kQuantRows;     // warps needed along M
+    int64_t gx = (row_steps + 7) / 8;
+    const int64_t cap = (int64_t(dev.num_sms) * 16 + pairs - 1) / pairs;  // about 16 CTAs per SM in total
+    if (gx > cap) gx = cap;
+    if (gx < 1) gx = 1;
+    quant_act_small_kernel<<<dim3(unsigned(gx), unsigned(pairs)), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(p.x), p.M, p.K, p.ldx, static_cast<uint8_t*>(p.a), p.lda, p.scales, p.lds);
+    return cudaGetLastError();
+  }
+  static bool attr_done[64] = {};
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if (device < 64 && !attr_done[device]) {
+    e = cudaFuncSetAttribute(quant_act_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kQSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done[device] = true;
+  }
+  const int64_t tiles = ((p.M + kQTileRows - 1) / kQTileRows) * (p.K / 128);
+  const int64_t slots = int64_t(dev.num_sms) * 2;   // two 97 KB CTAs per SM
+  const unsigned grid = unsigned(tiles < slots ? tiles : slots);
+  quant_act_kernel<<<grid, kQThreads, kQSmemBytes, s>>>(p.tmX, p.M, p.K, static_cast<uint8_t*>(p.a), p.lda,
+                                                        p.scales, p.lds, p.err);
   return cudaGetLastError();
 }
 
