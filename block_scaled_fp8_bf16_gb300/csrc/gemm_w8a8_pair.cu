@@ -34,7 +34,12 @@
 //                asynchronous; rows past M are clipped by the tensor map).
 // Tiles of the pair run persistently in grouped raster order ("Blockwise FP8
 // on Ada GPUs, part 2", "One tile doesn't fit all M": launch-order swizzle).
+// A last round that would leave at most half of the pairs busy runs its
+// tiles as 256 x 128 halves instead (MMA N = 128), so that it takes about
+// half as long.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -70,6 +75,7 @@ static_assert(kRegsWg0 * 128 + kRegsEpi * 256 <= kRegsLaunch * kThreads, "regist
 constexpr int kAccBufs = 2;
 constexpr uint32_t kTmemCols = kAccBufs * PN;
 constexpr uint32_t kIdesc = make_idesc(0 /* e4m3 */, 2 * TM, PN);
+constexpr uint32_t kIdescHalf = make_idesc(0 /* e4m3 */, 2 * TM, HN);   // a 256 x 128 half tile
 constexpr int kGroupM = 8;
 constexpr int kBarrierBytes = 1024;
 constexpr size_t kAsOff = size_t(kStages) * kStageBytes;
@@ -92,6 +98,31 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
   const int r = t - g * per_group;
   mt = first + r % gsz;
   nt = r / gsz;
+}
+
+// Work items of the persistent loop.  When the tiles leave a last round that
+// would keep at most half of the pairs busy, each of those last tiles runs as
+// two 256 x 128 halves on two pairs (MMA N = 128), which halves the length of
+// that round.  Items [0, full_items) are whole tiles; item full_items + 2u + h
+// is half h of tile full_items + u.  half = -1 marks a whole tile.
+struct Items {
+  int full_items, num_items;
+};
+__device__ __forceinline__ Items make_items(int num_tiles, int num_pairs) {
+  const int rem = num_tiles % num_pairs;
+  const int split = (num_tiles > num_pairs && rem > 0 && 2 * rem <= num_pairs) ? rem : 0;
+  return Items{num_tiles - split, num_tiles + split};
+}
+__device__ __forceinline__ void item_coords(int t, const Items& items, int m_tiles, int n_tiles, int& mt, int& nt,
+                                            int& half) {
+  if (t < items.full_items) {
+    tile_coords(t, m_tiles, n_tiles, mt, nt);
+    half = -1;
+  } else {
+    const int u = t - items.full_items;
+    tile_coords(items.full_items + (u >> 1), m_tiles, n_tiles, mt, nt);
+    half = u & 1;
+  }
 }
 
 __device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, int site) {
@@ -161,6 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = dempty + kAccBufs;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // The epilogue re-reads the item counts from here at each tile instead of
+  // keeping them in registers across its K loop.
+  volatile int* items_sh = abort_flag + 1;   // full_items, num_items
 
   griddep_launch_dependents();   // the next kernel may start its prologue; it gets an SM when this CTA leaves
 
@@ -172,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tiles = (M + 2 * TM - 1) / (2 * TM);
   const int n_tiles = (N + PN - 1) / PN;
   const int num_tiles = m_tiles * n_tiles;
+  const Items items = make_items(num_tiles, num_pairs);
   const int kblocks = K / BK;
 
   if (threadIdx.x == 0) {
@@ -189,6 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, kIssuers);
     *abort_flag = 0;
+    items_sh[0] = items.full_items;
+    items_sh[1] = items.num_items;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -220,11 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a_side) griddep_wait();
       uint32_t it = 0, gi = 0;   // operand items and scale groups issued
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        int mt, nt;
-        tile_coords(t, m_tiles, n_tiles, mt, nt);
+      for (int t = pair; t < items.num_items && ok; t += num_pairs) {
+        int mt, nt, half;
+        item_coords(t, items, m_tiles, n_tiles, mt, nt, half);
         const int m0 = mt * 2 * TM + rank * TM;
-        const int n0 = nt * PN + rank * HN;
+        // A half tile's MMA reads the first 64 of this CTA's B rows: rows
+        // 128 half + 64 rank of the tile (the box's other 64 rows go unused).
+        const int n0 = half < 0 ? nt * PN + rank * HN : nt * PN + half * HN + rank * (HN / 2);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
@@ -281,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t w = warp == 1 ? 0u : 1u;
       uint32_t it = 0;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+      for (int t = pair; t < items.num_items && ok; t += num_pairs) {
+        const uint32_t idesc = t < items.full_items ? kIdesc : kIdescHalf;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           if ((it & 1u) != w) continue;
           const int s = it % kStages;
@@ -303,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_tmem = tmem + w * uint32_t(PN);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
-            mma_f8_ss_pair(d_tmem, desc_sw128_kmajor(a0 + 32u * k), desc_sw128_kmajor(b0 + 32u * k), kIdesc,
+            mma_f8_ss_pair(d_tmem, desc_sw128_kmajor(a0 + 32u * k), desc_sw128_kmajor(b0 + 32u * k), idesc,
                            k > 0 ? 1u : 0u);
           }
           mma_commit_pair_mc(&empty[s], 0x3);
@@ -319,7 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ promotion + epilogue
     const int e = warp - 4;
     const int quarter = warp & 3;
-    const int col0 = (e >> 2) * kCols;
     const int row = quarter * 32 + lane;
     const uint32_t dempty0 = map_shared_rank(smem_u32(dempty), 0);
     uint8_t* stg = c_stage + size_t(e) * kBoxesPerWarp * kStageC;
@@ -327,14 +366,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     float2 acc[kCols / 2];
     uint32_t it = 0, gi = 0;   // K blocks and scale groups consumed
     bool ok = true;
-    for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-      int mt, nt;
-      tile_coords(t, m_tiles, n_tiles, mt, nt);
-      const int y = mt * 2 * TM + rank * TM + quarter * 32;   // first row of this warp's 32-row block
-      const int n = nt * PN + col0;
+    // One tile (NC = 128: half of a whole tile's 256 partial columns) or one
+    // half tile (NC = 64 of its 128); instantiated for both so that the
+    // whole-tile path keeps its column offsets as constants.
+    // y: first row of this warp's 32-row block; n_item: first output column
+    // of the tile or half tile.
+    auto promote = [&](auto nc_tag, int y, int n_item) {
+      constexpr int NC = decltype(nc_tag)::value;
+      const int col0 = (e >> 2) * NC;
+      const int n = n_item + col0;
       const bool col_ok = n < N;
 #pragma unroll
-      for (int j = 0; j < kCols / 2; ++j) acc[j] = make_float2(0.f, 0.f);
+      for (int j = 0; j < NC / 2; ++j) acc[j] = make_float2(0.f, 0.f);
       const float* bs_row = Bs + size_t(col_ok ? n / 128 : 0) * kblocks;
       float bs_win = 0.f;
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
@@ -347,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             !__all_sync(0xffffffffu, mbar_wait(&as_full[j], (gi / kAsStages) & 1u, abort_flag))) {
           raise_error(err, abort_flag, kSiteEpilogueFull);
           ok = false;
-          break;
+          return;
         }
         const float sa = as_stage[(j * kAsGroup + kb % kAsGroup) * TM + row];
         if (kb % kAsGroup == kAsGroup - 1 || kb == kblocks - 1) {
@@ -358,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(&dfull[d], dph, abort_flag))) {
           raise_error(err, abort_flag, kSiteEpilogueFull);
           ok = false;
-          break;
+          return;
         }
         tc_fence_after();
         const float sc = sa * sb;
@@ -366,12 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Two 32-column loads per wait; the buffer is handed back as soon as
         // the last columns are in registers.
 #pragma unroll
-        for (int c = 0; c < kCols / kChunk; c += 2) {
+        for (int c = 0; c < NC / kChunk; c += 2) {
           uint32_t p[2 * kChunk];
           tmem_ld_x32(taddr + uint32_t(c * kChunk), p);
           tmem_ld_x32(taddr + uint32_t((c + 1) * kChunk), p + kChunk);
           tmem_ld_wait();
-          if (c + 2 == kCols / kChunk) {
+          if (c + 2 == NC / kChunk) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(dempty0 + uint32_t(d) * 8u);
@@ -384,34 +427,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (ok && y < M && col_ok) {
-        // The warp's 32 x 128 block leaves as 128-byte-wide boxes (64 bf16 or
-        // 32 float32 columns), kBoxesPerWarp at a time through the staging
-        // boxes; chunk c (16 bytes) of row r sits at 16-byte position
-        // c ^ (r & 7) of the row (128-byte swizzle).
+      if (y < M && col_ok) {
+        // The warp's 32 x NC block leaves as 128-byte-wide boxes (64 bf16 or
+        // 32 float32 columns), at most kBoxesPerWarp at a time through the
+        // staging boxes; chunk c (16 bytes) of row r sits at 16-byte
+        // position c ^ (r & 7) of the row (128-byte swizzle).
         constexpr int kBoxCols = F32 ? 32 : 64;
-        constexpr int kRounds = kCols / kBoxCols / kBoxesPerWarp;
+        constexpr int kBoxes = NC / kBoxCols;
+        constexpr int kPer = kBoxes < kBoxesPerWarp ? kBoxes : kBoxesPerWarp;
 #pragma unroll
-        for (int r = 0; r < kRounds; ++r) {
+        for (int r = 0; r < kBoxes / kPer; ++r) {
           if (lane == 0) bulk_wait_group_read0();   // earlier stores have left the staging boxes
           __syncwarp();
 #pragma unroll
-          for (int h = 0; h < kBoxesPerWarp; ++h) {
+          for (int h = 0; h < kPer; ++h) {
             uint8_t* dst = stg + h * kStageC + lane * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(dst + ((c ^ (lane & 7)) << 4)) = out_chunk<F32>(acc, r * kBoxesPerWarp + h, c);
+              *reinterpret_cast<uint4*>(dst + ((c ^ (lane & 7)) << 4)) = out_chunk<F32>(acc, r * kPer + h, c);
           }
           fence_async_shared();   // generic-proxy writes become visible to the TMA engine
           __syncwarp();
           if (lane == 0) {
 #pragma unroll
-            for (int h = 0; h < kBoxesPerWarp; ++h)
-              tma_store_2d(&tmC, stg + h * kStageC, n + (r * kBoxesPerWarp + h) * kBoxCols, y);
+            for (int h = 0; h < kPer; ++h) tma_store_2d(&tmC, stg + h * kStageC, n + (r * kPer + h) * kBoxCols, y);
             bulk_commit_group();
           }
         }
       }
+    };
+    for (int t = pair; ok; t += num_pairs) {
+      const Items it_sh{items_sh[0], items_sh[1]};
+      if (t >= it_sh.num_items) break;
+      int mt, nt, half;
+      item_coords(t, it_sh, m_tiles, n_tiles, mt, nt, half);
+      const int y = mt * 2 * TM + rank * TM + quarter * 32;
+      if (half < 0)
+        promote(std::integral_constant<int, kCols>{}, y, nt * PN);
+      else
+        promote(std::integral_constant<int, kCols / 2>{}, y, nt * PN + half * HN);
     }
     if (lane == 0) bulk_wait_group0();   // the staging buffer stays valid until the stores are done
   }

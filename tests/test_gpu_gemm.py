@@ -45,9 +45,10 @@ def gpu_w8a8(a, As, b, Bs, ldc_pad=0, lds_pad=0):
     (128, 4096, 4096),     # split-K cluster path
     (1, 4096, 4096),
     (300, 1024, 1024),     # persistent path
-    (2200, 4992, 512),     # CTA-pair path, ragged M and a half-width last column tile
-    (1000, 2432, 1024),    # CTA-pair path
-    (513, 8192, 384),      # CTA-pair path, one row past a tile boundary
+    (2200, 4992, 512),     # CTA-pair path, ragged M, a half-width last column tile; 180 tiles: last 28 split
+    (1000, 2432, 1024),    # CTA-pair path, 40 tiles (no split last round)
+    (513, 8192, 384),      # CTA-pair path, one row past a tile boundary; 96 tiles: last 20 split in halves
+    (2304, 2304, 256),     # CTA-pair path, 81 tiles: the last 5 run as 10 half tiles
 ])
 def test_w8a8_matches_oracle(lib, M, N, K):
     a, As, b, Bs = w8a8_inputs(M + N + K, M, N, K)
