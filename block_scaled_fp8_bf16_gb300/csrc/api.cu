@@ -184,14 +184,11 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   if (st != FP8BLK_OK) return st;
   const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
   if (K == 0) return zero_output(c, ldc, M, N, f32 ? 4 : 2, s);
-  const bool decode = M <= kW8A16DecodeMaxM;
-  const int tile_m = decode ? (M <= 16 ? 16 : 32) : w8a16_pick_tile_m(M);
   GemmW8A16Args p;
-  st = make_map(p.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, uint64_t(K), uint64_t(N), uint64_t(ldb), 128, 128);
-  if (st != FP8BLK_OK) return st;
-  st = make_map(p.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, uint64_t(K), uint64_t(M), uint64_t(ldx) * 2, 64,
-                uint32_t(tile_m));
-  if (st != FP8BLK_OK) return st;
+  p.x = x;
+  p.ldx = ldx;
+  p.b = b;
+  p.ldb = ldb;
   p.scales = sc;
   p.fmt = fmt;
   p.C = c;
@@ -199,10 +196,21 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
-  p.tile_m = tile_m;
   p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
-  p.out_f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
+  p.out_f32 = f32;
   p.err = dev.err_word;
+  if (w8a16_use_gemv(M, N, K, dev)) {
+    p.tile_m = 0;
+    return cuda_status(launch_w8a16_gemv(p, dev, s));
+  }
+  const bool decode = M <= kW8A16DecodeMaxM;
+  const int tile_m = decode ? (M <= 16 ? 16 : 32) : w8a16_pick_tile_m(M);
+  st = make_map(p.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, uint64_t(K), uint64_t(N), uint64_t(ldb), 128, 128);
+  if (st != FP8BLK_OK) return st;
+  st = make_map(p.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, uint64_t(K), uint64_t(M), uint64_t(ldx) * 2, 64,
+                uint32_t(tile_m));
+  if (st != FP8BLK_OK) return st;
+  p.tile_m = tile_m;
   return cuda_status(decode ? launch_w8a16_decode(p, dev, s) : launch_gemm_w8a16(p, dev, s));
 }
 

@@ -31,12 +31,12 @@ def ref_w8a16(fmt, x, b, sc):
 
 # (M, N, K): comments give the work split the kernel picks on 152 SMs.
 @pytest.mark.parametrize("M,N,K", [
-    (1, 28672, 4096),    # clusters of 2, three tiles per cluster (per-tile cluster reductions)
-    (3, 28672, 1024),    # clusters of 2, three tiles per cluster, 4 K blocks per CTA
+    (3, 28672, 4096),    # clusters of 2, three tiles per cluster (per-tile cluster reductions)
+    (4, 28672, 1024),    # clusters of 2, three tiles per cluster, 4 K blocks per CTA
     (7, 16384, 2048),    # no split: one tile per CTA
     (24, 19968, 1152),   # token tile 32, clusters of 2 with 4 and 5 K blocks, several tiles each
     (32, 8192, 1024),    # token tile 32, clusters of 2
-    (1, 19456, 5120),    # no split, 40 K blocks per CTA: scale windows reloaded after 32 blocks
+    (3, 19456, 5120),    # no split, 40 K blocks per CTA: scale windows reloaded after 32 blocks
     (13, 128, 8192),     # one tile, clusters of 8
 ])
 @pytest.mark.parametrize("fmt", [0, 1])
@@ -65,13 +65,14 @@ def test_decode_repeatable(lib):
     assert all(torch.equal(outs[0], o) for o in outs[1:])
 
 
+@pytest.mark.parametrize("M", [1, 4])      # CUDA-core GEMV for the first product, decode-size kernel
 @pytest.mark.parametrize("fmt", [0, 1])
-def test_pdl_chain_reads_previous_output(lib, fmt):
+def test_pdl_chain_reads_previous_output(lib, fmt, M):
     """c1 = x W1, c2 = c1 W2, c1 = x' W1 again, all with FP8BLK_FLAG_PDL on one
     stream, repeated: every c2 must be the product of the c1 written just
     before it, and the later write of c1 must not reach the c2 that reads it."""
     import block_scaled_fp8_bf16_gb300 as fp8blk
-    M, N1, K1, N2 = 4, 8192, 4096, 2048
+    N1, K1, N2 = 8192, 4096, 2048
     x = [synth.activations(10 + i, M, K1) for i in range(2)]
     b1, s1 = weights(fmt, 20, N1, K1)
     b2, s2 = weights(fmt, 21, N2, N1)

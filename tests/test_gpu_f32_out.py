@@ -60,6 +60,8 @@ def test_w8a8_f32_out(lib, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K,fmt", [
+    (1, 256, 4096, 0),     # CUDA-core GEMV
+    (1, 640, 4224, 1),     # CUDA-core GEMV, a one-pass second segment
     (1, 256, 512, 0),      # decode-size kernel, 16-token tile
     (24, 384, 1024, 1),    # decode-size kernel, 32-token tile
     (5, 4096, 4096, 0),    # decode-size kernel, K split over a cluster
