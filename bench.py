@@ -585,6 +585,62 @@ def run_case(spec: str, iters: int):
         raise SystemExit("device error word set")
 
 
+# ---------------------------------------------------------------- probe
+
+def probe():
+    """Memory-system figures that frame the rooflines (no kernel of this
+    repository runs): device read, write and copy rates by size with torch
+    reductions, fills and copies, and the host link's copy-engine rates for
+    one 33.5 MB transfer (the headline step's activations or output), alone
+    and with both directions at once.  One JSON line per measurement."""
+    import torch
+    dev = torch.device("cuda:0")
+
+    def best(fn, reps=10):
+        fn()
+        torch.cuda.synchronize()
+        t = 1e9
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            t = min(t, a.elapsed_time(b) * 1e-3)
+        return t
+
+    for nbytes in (1 << 27, 1 << 29, 1 << 31):
+        a = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
+        b = torch.empty_like(a)
+        for what, fn, moved in (("read (sum)", lambda: a.sum(), nbytes), ("write (fill)", lambda: b.fill_(1.0), nbytes),
+                                ("copy (read + write)", lambda: b.copy_(a), 2 * nbytes)):
+            t = best(fn)
+            print(json.dumps({"probe": "hbm", "op": what, "mib": nbytes >> 20, "gb_s": round(moved / t / 1e9, 1)}))
+        del a, b
+    n = HEAD_M * HEAD_K * 2
+    h = [torch.empty(n, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    d = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    cur = torch.cuda.current_stream()
+
+    def both():
+        ev = torch.cuda.Event()
+        ev.record(cur)
+        for s, dst, src in ((s_in, d[0], h[0]), (s_out, h[1], d[1])):
+            s.wait_event(ev)
+            with torch.cuda.stream(s):
+                dst.copy_(src, non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    for what, fn in (("h2d", lambda: d[0].copy_(h[0], non_blocking=True)),
+                     ("d2h", lambda: h[1].copy_(d[1], non_blocking=True)),
+                     ("h2d + d2h at once (per direction)", both)):
+        t = best(fn)
+        print(json.dumps({"probe": "host link, pinned, copy engines", "op": what, "mb": round(n / 1e6, 1),
+                          "gb_s": round(n / t / 1e9, 1)}))
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -601,7 +657,12 @@ def main():
     ap.add_argument("--case", default=None, help="run one configuration untimed (w8a8:M,N,K | quant:M,K | "
                                                   "w8a16:M,N,K,fmt) for profiling")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--probe", action="store_true",
+                    help="print device-memory and host-link rates (torch operations only) and exit")
     args = ap.parse_args()
+    if args.probe:
+        probe()
+        return
     if args.case:
         import block_scaled_fp8_bf16_gb300 as fp8blk
         fp8blk._L()
