@@ -184,11 +184,25 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   if (st != FP8BLK_OK) return st;
   const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
   if (K == 0) return zero_output(c, ldc, M, N, f32 ? 4 : 2, s);
+  if (gemv_window(M, N, K, dev)) {
+    GemvArgs g;
+    g.x = x;
+    g.a_scales = nullptr;
+    g.lds = 0;
+    g.b = b;
+    g.ldb = ldb;
+    g.scales = sc;
+    g.fmt = fmt;
+    g.act = kGemvActBf16;
+    g.C = c;
+    g.N = int(N);
+    g.K = int(K);
+    g.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
+    g.out_f32 = f32;
+    g.err = dev.err_word;
+    return cuda_status(launch_gemv(g, dev, s));
+  }
   GemmW8A16Args p;
-  p.x = x;
-  p.ldx = ldx;
-  p.b = b;
-  p.ldb = ldb;
   p.scales = sc;
   p.fmt = fmt;
   p.C = c;
@@ -199,10 +213,6 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
   p.out_f32 = f32;
   p.err = dev.err_word;
-  if (w8a16_use_gemv(M, N, K, dev)) {
-    p.tile_m = 0;
-    return cuda_status(launch_w8a16_gemv(p, dev, s));
-  }
   const bool decode = M <= kW8A16DecodeMaxM;
   const int tile_m = decode ? (M <= 16 ? 16 : 32) : w8a16_pick_tile_m(M);
   st = make_map(p.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, uint64_t(K), uint64_t(N), uint64_t(ldb), 128, 128);
@@ -239,6 +249,24 @@ fp8blk_status run_w8a8(const void* a_e4m3, int64_t lda, const float* a_scales, i
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
   if (K == 0) return zero_output(c_bf16, ldc, M, N, f32 ? 4 : 2, s);
+  if (G == 0 && gemv_window(M, N, K, dev)) {
+    GemvArgs g;
+    g.x = a_e4m3;
+    g.a_scales = a_scales;
+    g.lds = lds;
+    g.b = b_e4m3;
+    g.ldb = ldb;
+    g.scales = b_scales;
+    g.fmt = 0;
+    g.act = kGemvActE4m3;
+    g.C = c_bf16;
+    g.N = int(N);
+    g.K = int(K);
+    g.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
+    g.out_f32 = f32;
+    g.err = dev.err_word;
+    return cuda_status(launch_gemv(g, dev, s));
+  }
   const int64_t b_rows = G > 0 ? G * N : N;
   GemmW8A8Args p;
   std::memset(&p.tmX, 0, sizeof(p.tmX));     // read only by the fused form
@@ -338,6 +366,24 @@ fp8blk_status fp8blk_linear_w8a8(const void* x_bf16, int64_t ldx, const void* b_
   if (st != FP8BLK_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return zero_output(c_bf16, ldc, M, N, f32 ? 4 : 2, s);
+  if (gemv_window(M, N, K, dev)) {
+    GemvArgs g;
+    g.x = x_bf16;
+    g.a_scales = nullptr;
+    g.lds = 0;
+    g.b = b_e4m3;
+    g.ldb = ldb;
+    g.scales = b_scales;
+    g.fmt = 0;
+    g.act = kGemvActQuant;
+    g.C = c_bf16;
+    g.N = int(N);
+    g.K = int(K);
+    g.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
+    g.out_f32 = f32;
+    g.err = dev.err_word;
+    return cuda_status(launch_gemv(g, dev, s));
+  }
   GemmW8A8Args p;
   std::memset(&p.tmA, 0, sizeof(p.tmA));     // not read by the fused form
   std::memset(&p.tmAs, 0, sizeof(p.tmAs));

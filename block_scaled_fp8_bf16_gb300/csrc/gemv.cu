@@ -1,4 +1,6 @@
-// W8A16 for a single token on the CUDA cores (sm_103a).
+// One-token products on the CUDA cores (sm_103a): W8A16 (bf16 token), W8A8
+// (e4m3 token codes with their 1x128 scales) and the W8A8 linear that
+// quantises the bf16 token itself.
 //
 // With M = 1 every weight byte carries one multiply-add, so the product is a
 // stream of the weight matrix past the token: its time is the DRAM time of
@@ -7,19 +9,23 @@
 // "SM70 FP8 block-32 kernels (PLI Labs)", "How it works": a GEMV that decodes
 // in registers and accumulates in FP32 serves the smallest M).  One token
 // fills no tensor-core tile, and on weight sets of up to ~32 MB the MMA
-// path's setup (TMEM, barriers, split-K reduction) costs more than the
-// stream.  The kernel is written for M tokens; only M = 1 is instantiated,
-// because at M = 2 the decode-size tensor-core kernel costs what it costs at
-// M = 1 while the arithmetic here doubles.
+// kernels' setup (TMEM, barriers, split-K reduction) costs more than the
+// stream.
 //
 // Arithmetic (the sums of the tensor-core kernels, in another order):
-//   * a code pair becomes two f16 values with cvt.rn.f16x2.e4m3x2, exactly
-//     (every finite e4m3 value is an f16 normal), then two f32 values;
-//   * a lane sums the 16 products x * w of its chunk in f32 (x staged once
-//     per CTA in shared memory as f32, which holds every bf16 exactly),
-//     multiplies the partial by the scale of the chunk's weight block -- the
-//     fp32 scale of the 128 x 128 block, or 2^(e - 127) for the UE8M0 byte e
-//     of the 32 x 32 block -- and accumulates;
+//   * the token is staged once per CTA in shared memory as f32: bf16 values
+//     exactly; e4m3 codes decoded exactly; or, for the quantising form, the
+//     codes of the 1x128 quantisation with the stand-alone quantiser's
+//     arithmetic (quant.cuh: amax, s = amax / 448, correctly rounded
+//     quotient, e4m3 round-to-nearest-even with saturation), decoded;
+//   * a weight code pair becomes two f16 values with cvt.rn.f16x2.e4m3x2,
+//     exactly (every finite e4m3 value is an f16 normal), then two f32 values;
+//   * a lane sums the 16 products of its chunk in f32 (products of e4m3 or
+//     bf16 values are exact in f32), multiplies the partial by the weight
+//     block's scale -- the fp32 scale of the 128 x 128 block, or 2^(e - 127)
+//     for the UE8M0 byte e of the 32 x 32 block -- times, for W8A8, the
+//     token's scale of the 128-block, and accumulates ("Blockwise FP8 on Ada
+//     GPUs, part 2", "The fix": one promotion per 128-K block);
 //   * at the end of a row the 32 lanes' sums are added with shuffles.
 // A 16-code chunk never straddles a scale block (16 divides 32 and 128).
 //
@@ -32,18 +38,19 @@
 // warp has used segment c, so S segments per warp are always on their way
 // and no other warp or barrier is involved.  Per segment a warp makes 8
 // passes of 512 codes (16 per lane).  The first S segments of every warp are
-// requested before griddepcontrol.wait; the tokens are read and the output
+// requested before griddepcontrol.wait; the token is read and the output
 // written after it.
 //
-// Shared-memory layout: x as f32 [M][K] (16-byte unit u of a token stored at
-// unit u ^ ((u >> 2) & 7), so that the eight lanes of one 16-byte-load phase,
-// whose chunks are 64 bytes apart, fall in eight different bank groups), then
-// the slots, then one barrier per slot.
+// Shared-memory layout: the token as f32 [K] (16-byte unit u stored at unit
+// u ^ ((u >> 2) & 7), so that the eight lanes of one 16-byte-load phase,
+// whose chunks are 64 bytes apart, fall in eight different bank groups), the
+// token's K / 128 scales (W8A8 forms), the slots, then one barrier per slot.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace fp8blk {
 namespace {
@@ -52,10 +59,10 @@ constexpr int kChunk = 16;              // codes per lane per pass
 constexpr int kPass = 32 * kChunk;      // codes per warp pass
 constexpr int kSeg = 4096;              // codes per slot (8 passes)
 constexpr int kPasses = kSeg / kPass;
-constexpr int kConsumers = 16;          // warps
-constexpr int kThreads = kConsumers * 32;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSlotsPerWarp = 6;
-constexpr int kMaxStages = kConsumers * kMaxSlotsPerWarp;
+constexpr int kMaxStages = kWarps * kMaxSlotsPerWarp;
 constexpr int kBarrierBytes = kMaxStages * 8 + 16;
 constexpr int kMinSlotsPerWarp = 2;
 
@@ -71,6 +78,10 @@ struct SegScales {
 static_assert(kSeg == 32 * 128, "a segment spans 32 blocks of 128 codes");
 
 __host__ __device__ constexpr int slot_bytes(int K) { return K < kSeg ? K : kSeg; }
+
+// Bytes of the token area: K f32 values, then K / 128 f32 scales rounded up
+// to 128 bytes (the slots after it need 16-byte alignment).
+__host__ __device__ constexpr int64_t token_bytes(int64_t K) { return K * 4 + ((K / 128 * 4 + 127) / 128) * 128; }
 
 // Bulk copy of `bytes` (a multiple of 16) global -> shared, completing on bar.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
@@ -92,6 +103,13 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
   return __half22float2(hh);
 }
 
+// Four codes (byte i = element i) -> one float4, exactly.
+__device__ __forceinline__ float4 e4m3x4_to_f32x4(uint32_t four_codes) {
+  const float2 lo = e4m3x2_to_f32x2(four_codes);
+  const float2 hi = e4m3x2_to_f32x2(four_codes >> 16);
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
 // Scale of K block kb (of SegScales<FMT>::kBlock codes) in weight row n.
 template <int FMT>
 __device__ __forceinline__ float block_scale(const void* scales, int n, int kb, int K) {
@@ -103,17 +121,63 @@ __device__ __forceinline__ float block_scale(const void* scales, int n, int kb, 
   }
 }
 
-template <int M, class OutT, int FMT>
+// Stages the token into shared memory as f32 (and, for the W8A8 forms, its
+// K / 128 scales).  All threads of the CTA take part.
+template <int ACT>
+__device__ __forceinline__ void stage_token(const void* x, const float* a_scales, int64_t lds, int K, float4* xs4,
+                                            float* as_sm) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if constexpr (ACT == kGemvActBf16) {
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    for (int i = threadIdx.x; i < K / 8; i += blockDim.x) {
+      float f[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(xb + 8 * i), f);
+      xs4[x_unit(2 * i)] = make_float4(f[0], f[1], f[2], f[3]);
+      xs4[x_unit(2 * i + 1)] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+  } else if constexpr (ACT == kGemvActE4m3) {
+    const uint8_t* a = static_cast<const uint8_t*>(x);
+    for (int i = threadIdx.x; i < K / 16; i += blockDim.x) {
+      const uint4 v = *reinterpret_cast<const uint4*>(a + 16 * i);
+      xs4[x_unit(4 * i)] = e4m3x4_to_f32x4(v.x);
+      xs4[x_unit(4 * i + 1)] = e4m3x4_to_f32x4(v.y);
+      xs4[x_unit(4 * i + 2)] = e4m3x4_to_f32x4(v.z);
+      xs4[x_unit(4 * i + 3)] = e4m3x4_to_f32x4(v.w);
+    }
+    for (int g = threadIdx.x; g < K / 128; g += blockDim.x) as_sm[g] = a_scales[int64_t(g) * lds];
+  } else {
+    // One warp per 128-group, four values per lane.
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    for (int g = warp; g < K / 128; g += kWarps) {
+      const uint2 v = *reinterpret_cast<const uint2*>(xb + g * 128 + 4 * lane);
+      const float f0 = __uint_as_float(v.x << 16), f1 = __uint_as_float(v.x & 0xFFFF0000u);
+      const float f2 = __uint_as_float(v.y << 16), f3 = __uint_as_float(v.y & 0xFFFF0000u);
+      float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float s = group_scale(amax);
+      const Divisor d = make_divisor(s);
+      const uint32_t q = e4m3x4(quotient(f0, d), quotient(f1, d), quotient(f2, d), quotient(f3, d));
+      xs4[x_unit(g * 32 + lane)] = e4m3x4_to_f32x4(q);
+      if (lane == 0) as_sm[g] = s;
+    }
+  }
+}
+
+template <int ACT, class OutT, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemv_w8a16_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, const uint8_t* __restrict__ b, int64_t ldb,
-                      const void* __restrict__ scales, OutT* __restrict__ c, int64_t ldc, int N, int K,
-                      int slots_per_warp, int* __restrict__ err) {
+    gemv_kernel(const void* __restrict__ x, const float* __restrict__ a_scales, int64_t lds,
+                const uint8_t* __restrict__ b, int64_t ldb, const void* __restrict__ scales, OutT* __restrict__ c,
+                int N, int K, int slots_per_warp, int* __restrict__ err) {
+  static_assert(ACT == kGemvActBf16 || FMT == 0, "W8A8 weights carry fp32 128x128 scales");
   extern __shared__ __align__(128) uint8_t smem[];
   float4* xs4 = reinterpret_cast<float4*>(smem);
+  float* as_sm = reinterpret_cast<float*>(smem + size_t(K) * 4);
   const int slot = slot_bytes(K);
-  uint8_t* stages = smem + size_t(M) * K * 4;
+  uint8_t* stages = smem + token_bytes(K);
   const int S = slots_per_warp;
-  uint64_t* full = reinterpret_cast<uint64_t*>(stages + size_t(kConsumers) * S * slot);
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + size_t(kWarps) * S * slot);
   griddep_launch_dependents();
 
   const int warp = threadIdx.x >> 5;
@@ -122,16 +186,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows = int(int64_t(blockIdx.x + 1) * N / gridDim.x) - row0;
   const int nseg = (K + kSeg - 1) / kSeg;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kConsumers * S; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kWarps * S; ++i) mbar_init(&full[i], 1);
     fence_mbar_init();
   }
   __syncthreads();
 
-  // Segment c of this warp is segment c % nseg of row warp + kConsumers *
+  // Segment c of this warp is segment c % nseg of row warp + kWarps *
   // (c / nseg), in slot warp * S + c % S, use c / S of that slot.
   const uint64_t policy = policy_evict_first();
   auto request = [&](int c) {   // one lane
-    const int j = warp + kConsumers * (c / nseg);
+    const int j = warp + kWarps * (c / nseg);
     if (j >= rows) return;
     const int seg = c % nseg;
     const int sl = warp * S + c % S;
@@ -144,35 +208,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (lane == 0)
     for (int c = 0; c < S; ++c) request(c);
 
-  // Tokens: bf16 -> f32 into shared memory, eight values per thread step.
-  griddep_wait();
-  const int units8 = K / 8;
-  for (int i = threadIdx.x; i < M * units8; i += blockDim.x) {
-    const int m = i / units8;
-    const int k = (i - m * units8) * 8;
-    const uint4 v = *reinterpret_cast<const uint4*>(x + int64_t(m) * ldx + k);
-    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-    float f[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[2 * j] = __uint_as_float(q[j] << 16);
-      f[2 * j + 1] = __uint_as_float(q[j] & 0xFFFF0000u);
-    }
-    float4* xm = xs4 + size_t(m) * (K / 4);
-    xm[x_unit(k / 4)] = make_float4(f[0], f[1], f[2], f[3]);
-    xm[x_unit(k / 4 + 1)] = make_float4(f[4], f[5], f[6], f[7]);
-  }
+  griddep_wait();   // the token may be the previous kernel's output
+  stage_token<ACT>(x, a_scales, lds, K, xs4, as_sm);
   __syncthreads();
 
-  // -------------------------------------------------------------- arithmetic
   constexpr int kSRegs = SegScales<FMT>::kRegs;
   constexpr int kBlock = SegScales<FMT>::kBlock;
   const int nblocks = K / kBlock;
-  for (int j = warp, r = 0; j < rows; j += kConsumers, ++r) {
+  for (int j = warp, r = 0; j < rows; j += kWarps, ++r) {
     const int n = row0 + j;
-    float acc[M];
-#pragma unroll
-    for (int m = 0; m < M; ++m) acc[m] = 0.f;
+    float acc = 0.f;
     bool ok = true;
     for (int seg = 0; seg < nseg; ++seg) {
       const int cs = r * nseg + seg;   // this warp's stage
@@ -189,10 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Nothing else waits on this warp: it reports and leaves after the
         // copies it requested have landed (each wait bounded).
         if (lane == 0) {
-          atomicCAS(err, 0, kDevErrW8A16Gemv | kSiteDecodeFull);
+          atomicCAS(err, 0, kDevErrGemv | kSiteDecodeFull);
           for (int c = cs; c < cs + S; ++c)
-            if (warp + kConsumers * (c / nseg) < rows)
-              mbar_wait(&full[warp * S + c % S], uint32_t((c / S) & 1), nullptr);
+            if (warp + kWarps * (c / nseg) < rows) mbar_wait(&full[warp * S + c % S], uint32_t((c / S) & 1), nullptr);
         }
         ok = false;
         break;
@@ -210,27 +254,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // This chunk's block within the segment: 4u + lane / 8 (fp32 format)
         // or 16u + lane / 2 (UE8M0); every lane takes part in the shuffle.
         const int gb = FMT == 0 ? 4 * u + (lane >> 3) : 16 * u + (lane >> 1);
-        const float su = __shfl_sync(0xffffffffu, sreg[gb >> 5], gb & 31);
+        float su = __shfl_sync(0xffffffffu, sreg[gb >> 5], gb & 31);
         if (k0 < bytes) {
+          if constexpr (ACT != kGemvActBf16) su *= as_sm[seg * (kSeg / 128) + gb];
           const uint32_t q[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-          const int ux = (seg * kSeg + k0) / 4;   // first 16-byte unit of x for this chunk
+          const int ux = (seg * kSeg + k0) / 4;   // first 16-byte unit of the token for this chunk
           // Packed f32x2 multiply-adds: even and odd k in the two halves.
-          float2 part[M];
-#pragma unroll
-          for (int m = 0; m < M; ++m) part[m] = make_float2(0.f, 0.f);
+          float2 part = make_float2(0.f, 0.f);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const float2 lo = e4m3x2_to_f32x2(q[jj]);
             const float2 hi = e4m3x2_to_f32x2(q[jj] >> 16);
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-              const float4 xv = xs4[size_t(m) * (K / 4) + x_unit(ux + jj)];
-              part[m] = ffma2(lo, make_float2(xv.x, xv.y), part[m]);
-              part[m] = ffma2(hi, make_float2(xv.z, xv.w), part[m]);
-            }
+            const float4 xv = xs4[x_unit(ux + jj)];
+            part = ffma2(lo, make_float2(xv.x, xv.y), part);
+            part = ffma2(hi, make_float2(xv.z, xv.w), part);
           }
-#pragma unroll
-          for (int m = 0; m < M; ++m) acc[m] = fmaf(part[m].x + part[m].y, su, acc[m]);
+          acc = fmaf(part.x + part.y, su, acc);
         }
       }
       // Every lane's codes have been used: the slot takes segment cs + S.
@@ -239,34 +278,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) break;
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-      float v = acc[m];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) {
-        if constexpr (sizeof(OutT) == 4)
-          c[int64_t(m) * ldc + n] = v;
-        else
-          c[int64_t(m) * ldc + n] = __float2bfloat16_rn(v);
-      }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      if constexpr (sizeof(OutT) == 4)
+        c[n] = acc;
+      else
+        c[n] = __float2bfloat16_rn(acc);
     }
   }
 }
 
-// Slots per consumer warp that fit next to the f32 tokens (0 if none).
-int gemv_slots_per_warp(int64_t M, int64_t K, int smem_optin) {
-  const int64_t avail = int64_t(smem_optin) - M * K * 4 - kBarrierBytes;
+// Slots per warp that fit next to the staged token (0 if none).
+int gemv_slots_per_warp(int64_t K, int smem_optin) {
+  const int64_t avail = int64_t(smem_optin) - token_bytes(K) - kBarrierBytes;
   if (avail <= 0) return 0;
-  const int64_t n = avail / (int64_t(kConsumers) * slot_bytes(int(K < kSeg ? K : kSeg)));
+  const int64_t n = avail / (int64_t(kWarps) * slot_bytes(int(K < kSeg ? K : kSeg)));
   return int(n < kMaxSlotsPerWarp ? n : kMaxSlotsPerWarp);
 }
 
-template <int M, class OutT, int FMT>
-cudaError_t launch_typed(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t stream) {
-  auto kernel = gemv_w8a16_kernel<M, OutT, FMT>;
-  const int spw = gemv_slots_per_warp(M, p.K, dev.max_smem_optin);
+template <int ACT, class OutT, int FMT>
+cudaError_t launch_typed(const GemvArgs& p, const DeviceInfo& dev, cudaStream_t stream) {
+  auto kernel = gemv_kernel<ACT, OutT, FMT>;
+  const int spw = gemv_slots_per_warp(p.K, dev.max_smem_optin);
   if (spw < kMinSlotsPerWarp) return cudaErrorInvalidValue;
-  const size_t smem = size_t(M) * p.K * 4 + size_t(kConsumers) * spw * slot_bytes(p.K) + kBarrierBytes;
+  const size_t smem = size_t(token_bytes(p.K)) + size_t(kWarps) * spw * slot_bytes(p.K) + kBarrierBytes;
   static bool attr_done[64] = {};
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
@@ -288,27 +323,33 @@ cudaError_t launch_typed(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<const __nv_bfloat16*>(p.x), p.ldx,
-                            static_cast<const uint8_t*>(p.b), p.ldb, p.scales, static_cast<OutT*>(p.C), p.ldc, p.N,
-                            p.K, spw, p.err);
+  return cudaLaunchKernelEx(&cfg, kernel, p.x, p.a_scales, p.lds, static_cast<const uint8_t*>(p.b), p.ldb,
+                            p.scales, static_cast<OutT*>(p.C), p.N, p.K, spw, p.err);
 }
 
-template <int M>
-cudaError_t launch_m(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t s) {
-  if (p.out_f32)
-    return p.fmt == 0 ? launch_typed<M, float, 0>(p, dev, s) : launch_typed<M, float, 1>(p, dev, s);
-  return p.fmt == 0 ? launch_typed<M, __nv_bfloat16, 0>(p, dev, s) : launch_typed<M, __nv_bfloat16, 1>(p, dev, s);
+template <int ACT, int FMT>
+cudaError_t launch_act(const GemvArgs& p, const DeviceInfo& dev, cudaStream_t s) {
+  return p.out_f32 ? launch_typed<ACT, float, FMT>(p, dev, s) : launch_typed<ACT, __nv_bfloat16, FMT>(p, dev, s);
 }
 
 }  // namespace
 
-bool w8a16_use_gemv(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+bool gemv_window(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   return M == 1 && K >= kSeg && N * K <= (int64_t(1) << 25) &&
-         gemv_slots_per_warp(M, K, dev.max_smem_optin) >= kMinSlotsPerWarp;
+         gemv_slots_per_warp(K, dev.max_smem_optin) >= kMinSlotsPerWarp;
 }
 
-cudaError_t launch_w8a16_gemv(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t s) {
-  return p.M == 1 ? launch_m<1>(p, dev, s) : cudaErrorInvalidValue;
+cudaError_t launch_gemv(const GemvArgs& p, const DeviceInfo& dev, cudaStream_t s) {
+  switch (p.act) {
+    case kGemvActBf16:
+      return p.fmt == 0 ? launch_act<kGemvActBf16, 0>(p, dev, s) : launch_act<kGemvActBf16, 1>(p, dev, s);
+    case kGemvActE4m3:
+      return p.fmt == 0 ? launch_act<kGemvActE4m3, 0>(p, dev, s) : cudaErrorInvalidValue;
+    case kGemvActQuant:
+      return p.fmt == 0 ? launch_act<kGemvActQuant, 0>(p, dev, s) : cudaErrorInvalidValue;
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fp8blk

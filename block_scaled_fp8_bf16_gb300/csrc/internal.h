@@ -16,7 +16,7 @@ enum DeviceErr : int {
   kDevErrW8A16 = 0x200,
   kDevErrW8A16Decode = 0x300,
   kDevErrQuant = 0x400,
-  kDevErrW8A16Gemv = 0x500,
+  kDevErrGemv = 0x500,
 };
 enum WaitSite : int {
   kSiteProducerEmpty = 1,
@@ -109,10 +109,6 @@ cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, 
 struct GemmW8A16Args {
   CUtensorMap tmW;    // e4m3 [N, K], box {128 (K), 128 (N)}, 128B swizzle
   CUtensorMap tmX;    // bf16 [M, K], box {64 (K), tile_m (M)}, 128B swizzle
-  const void* x;      // bf16 [M, K] pitch ldx (the CUDA-core GEMV reads it directly)
-  int64_t ldx;
-  const void* b;      // e4m3 [N, K] pitch ldb
-  int64_t ldb;
   const void* scales; // fp32 [N/128][K/128] or uint8 [N/32][K/32]
   int fmt;            // 0 = fp32 128x128, 1 = UE8M0 32x32
   void* C;
@@ -132,15 +128,35 @@ cudaError_t launch_gemm_w8a16(const GemmW8A16Args& p, const DeviceInfo& dev, cud
 constexpr int kW8A16DecodeMaxM = 32;
 cudaError_t launch_w8a16_decode(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t s);
 
-// One token: CUDA-core GEMV streaming the weight rows through per-warp rings
-// of shared-memory slots (no tensor maps; x is staged as f32 in shared
-// memory next to two slots per warp).  Chosen where the sweep measured it
-// faster than the decode-size kernel: M = 1, K >= 4096 and at most 2^25
-// weight codes; on larger weight sets the decode-size kernel streams faster,
-// and at M = 2 it costs the same as at M = 1 while the GEMV's arithmetic
-// doubles.
-bool w8a16_use_gemv(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
-cudaError_t launch_w8a16_gemv(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t s);
+// ------------------------------------------------------------------ one token
+// CUDA-core GEMV (gemv.cu) streaming the weight rows through per-warp rings
+// of shared-memory slots, the token staged as f32 in shared memory.  Chosen
+// where the sweep measured it faster than the tensor-core kernels: M = 1,
+// K >= 4096 and at most 2^25 weight codes; on larger weight sets the
+// tensor-core kernels stream faster, and at M = 2 the decode-size kernel
+// costs what it costs at M = 1 while the GEMV's arithmetic doubles.
+enum GemvAct : int {
+  kGemvActBf16 = 0,    // W8A16: x is a bf16 row
+  kGemvActE4m3 = 1,    // W8A8: x is an e4m3 row, its scales a_scales[kb * lds]
+  kGemvActQuant = 2,   // W8A8 linear: x is a bf16 row, quantised 1x128 in the kernel
+};
+struct GemvArgs {
+  const void* x;
+  const float* a_scales;   // kGemvActE4m3 only
+  int64_t lds;
+  const void* b;           // e4m3 [N, K] pitch ldb
+  int64_t ldb;
+  const void* scales;      // fp32 [N/128][K/128] or uint8 [N/32][K/32]
+  int fmt;                 // 0 = fp32 128x128, 1 = UE8M0 32x32 (W8A16 only)
+  int act;                 // GemvAct
+  void* C;                 // bf16 or float32 [N]
+  int N, K;
+  bool pdl;
+  bool out_f32;
+  int* err;
+};
+bool gemv_window(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
+cudaError_t launch_gemv(const GemvArgs& p, const DeviceInfo& dev, cudaStream_t s);
 
 // Work split of the decode kernel: K is divided over clusters of `split`
 // CTAs (1, 2, 4 or 8) and the 128-row weight tiles run persistently over

@@ -126,14 +126,30 @@ def test_pdl_w8a8_after_quant(lib):
             assert_gemm_close(bf16_out_to_f64(outs[r])[rows], ref, f"pdl w8a8 round {r}")
 
 
-def test_pdl_w8a8_decode_size(lib):
-    """Decode-size W8A8 (the split-K kernel) with the flag, after quant_act."""
+@pytest.mark.parametrize("M", [1, 3])      # one-token GEMV, split-K kernel
+def test_pdl_w8a8_decode_size(lib, M):
+    """Decode-size W8A8 with the flag, after quant_act, alternating two token
+    batches so that each product must read the codes written just before it;
+    the fused linear with the flag as well."""
     import block_scaled_fp8_bf16_gb300 as fp8blk
-    M, N, K = 3, 4096, 4096
-    x = synth.activations(40, M, K)
+    N, K = 4096, 4096
+    xs = [synth.activations(40 + i, M, K) for i in range(2)]
+    xd = [to_dev_bf16(v) for v in xs]
     b, Bs = O.quant_weight_128x128(synth.weights_bf16(41, N, K))
-    a, s = fp8blk.quant_act(to_dev_bf16(x))
-    out = fp8blk.gemm_w8a8(a, s, to_dev(b), to_dev(Bs), flags=fp8blk.FLAG_PDL)
+    bd, bsd = to_dev(b), to_dev(Bs)
+    a = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    s = torch.empty((K // 128, fp8blk.act_scales_pitch(M)), dtype=torch.float32, device="cuda")
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    lins = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    for r in range(4):
+        fp8blk.fp8blk_quant_act(xd[r % 2], a, s)
+        fp8blk.fp8blk_gemm_w8a8(a, s, bd, bsd, outs[r], flags=fp8blk.FLAG_PDL)
+        fp8blk.fp8blk_linear_w8a8(xd[r % 2], bd, bsd, lins[r], flags=fp8blk.FLAG_PDL)
     torch.cuda.synchronize()
-    a_ref, as_ref = O.quant_act_1x128(x)
-    assert_gemm_close(bf16_out_to_f64(out), O.gemm_w8a8(a_ref, as_ref, b, Bs), "pdl w8a8 decode")
+    assert fp8blk.fp8blk_device_error() == 0
+    for i in range(2):
+        a_ref, as_ref = O.quant_act_1x128(xs[i])
+        ref = O.gemm_w8a8(a_ref, as_ref, b, Bs)
+        for r in range(i, 4, 2):
+            assert_gemm_close(bf16_out_to_f64(outs[r]), ref, f"pdl w8a8 decode round {r}")
+            assert torch.equal(outs[r], lins[r]), f"pdl linear round {r}"

@@ -44,6 +44,7 @@ def _check_pair(c16, c32, ref, what):
 @pytest.mark.parametrize("M,N,K", [
     (16, 256, 512),        # single-CTA kernel, split-K cluster
     (129, 384, 1024),      # single-CTA kernel, ragged second row tile
+    (1, 640, 4224),        # one-token GEMV
     (1000, 2432, 1024),    # CTA-pair kernel, half-width last column tile
     (2200, 4992, 512),     # CTA-pair kernel, last-round tiles split in 256 x 128 halves
 ])

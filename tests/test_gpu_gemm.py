@@ -43,7 +43,10 @@ def gpu_w8a8(a, As, b, Bs, ldc_pad=0, lds_pad=0):
     (129, 256, 2048),      # ragged second row tile
     (255, 512, 512),
     (128, 4096, 4096),     # split-K cluster path
-    (1, 4096, 4096),
+    (1, 4096, 4096),       # one-token GEMV
+    (1, 384, 4224),        # one-token GEMV: a whole segment and a one-pass segment
+    (1, 2048, 14336),      # one-token GEMV: three segments and a half
+    (1, 8192, 4352),       # past the GEMV's weight-set limit: split-K kernel
     (300, 1024, 1024),     # persistent path
     (2200, 4992, 512),     # CTA-pair path, ragged M, a half-width last column tile; 180 tiles: last 28 split
     (1000, 2432, 1024),    # CTA-pair path, 40 tiles (no split last round)

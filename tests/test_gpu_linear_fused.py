@@ -1,7 +1,8 @@
 """The decode-size W8A8 linear with the activation quantisation inside the
-GEMM kernel: bit for bit equal to fp8blk_quant_act followed by
-fp8blk_gemm_w8a8 (same codes, same scales, same accumulation), and within
-the GEMM tolerance of the float64 oracle of quantisation + product."""
+GEMM kernel (the split-K kernel, or the one-token GEMV): bit for bit equal
+to fp8blk_quant_act followed by fp8blk_gemm_w8a8 (same codes, same scales,
+same accumulation), and within the GEMM tolerance of the float64 oracle of
+quantisation + product."""
 import numpy as np
 import pytest
 import torch
@@ -18,7 +19,8 @@ pytestmark = pytest.mark.gpu
     (16, 256, 512, torch.bfloat16),       # the tiny workload
     (32, 384, 1024, torch.bfloat16),
     (7, 4096, 4096, torch.bfloat16),      # K split over a cluster
-    (1, 4096, 4096, torch.float32),
+    (1, 4096, 4096, torch.float32),       # one-token GEMV quantising its token
+    (1, 2048, 8320, torch.bfloat16),      # one-token GEMV, a partial third segment
     (29, 1024, 2048, torch.float32),
 ])
 def test_fused_linear_equals_two_step_and_oracle(lib, M, N, K, dtype):
