@@ -29,7 +29,9 @@ namespace {
 // Activation quantiser, persistent and fed by TMA.  A tile is 64 token rows
 // of one 128-wide group (16 KB of bf16); tile t covers rows 64 (t / G) ..
 // and group t % G (G = K / 128).  One producer thread keeps kQStages tiles
-// in flight per CTA.  Eight warps consume a tile: warp w takes rows
+// in flight per CTA, three CTAs per SM (12 tiles, 192 KB, in flight per SM:
+// more consuming warps per SM than two CTAs of six tiles, for the same bytes
+// in flight).  Eight warps consume a tile: warp w takes rows
 // 8w .. 8w + 7, four lanes per row and 32 bf16 per lane (four 8-column
 // chunks, 32 columns apart, so a row's lanes read consecutive bytes), so the per-group
 // work (the row's amax from two xor shuffles, the IEEE scale division and
@@ -39,7 +41,8 @@ namespace {
 constexpr int kQTileRows = kQuantTileRows;
 constexpr int64_t kQuantSmallM = 256;   // up to this many rows the register-fed kernel below runs
 constexpr int kQTileBytes = kQTileRows * 128 * 2;
-constexpr int kQStages = 6;
+constexpr int kQStages = 4;
+constexpr int kQCtasPerSm = 3;
 constexpr int kQWarps = 8;
 constexpr int kQThreads = (kQWarps + 1) * 32;
 constexpr size_t kQSmemBytes = size_t(kQStages) * kQTileBytes + 2 * kQStages * 8 + 1024;
@@ -49,7 +52,7 @@ __device__ __forceinline__ void quant_raise(int* err, volatile int* abort_flag, 
   atomicCAS(err, 0, kDevErrQuant | site);
 }
 
-__global__ void __launch_bounds__(kQThreads) quant_act_kernel(const __grid_constant__ CUtensorMap tmX, int64_t M,
+__global__ void __launch_bounds__(kQThreads, kQCtasPerSm) quant_act_kernel(const __grid_constant__ CUtensorMap tmX, int64_t M,
                                                               int64_t K, uint8_t* __restrict__ a, int64_t lda,
                                                               float* __restrict__ scales, int64_t lds,
                                                               int* __restrict__ err) {
@@ -324,7 +327,7 @@ cudaError_t launch_quant_act(const QuantActArgs& p, const DeviceInfo& dev, cudaS
     attr_done[device] = true;
   }
   const int64_t tiles = ((p.M + kQTileRows - 1) / kQTileRows) * (p.K / 128);
-  const int64_t slots = int64_t(dev.num_sms) * 2;   // two 97 KB CTAs per SM
+  const int64_t slots = int64_t(dev.num_sms) * kQCtasPerSm;
   const unsigned grid = unsigned(tiles < slots ? tiles : slots);
   quant_act_kernel<<<grid, kQThreads, kQSmemBytes, s>>>(p.tmX, p.M, p.K, static_cast<uint8_t*>(p.a), p.lda,
                                                         p.scales, p.lds, p.err);
