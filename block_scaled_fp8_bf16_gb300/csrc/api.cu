@@ -177,6 +177,28 @@ fp8blk_status zero_output(void* c, int64_t ldc, int64_t M, int64_t N, int64_t el
   return cuda_status(cudaMemset2DAsync(c, size_t(ldc * elem), 0, size_t(N * elem), size_t(M), s));
 }
 
+// One-token products on the CUDA-core GEMV (see gemv_window for when).
+fp8blk_status run_gemv(int act, const void* x, const float* a_scales, int64_t lds, const void* b, int64_t ldb,
+                       const void* sc, int fmt, void* c, int64_t N, int64_t K, uint32_t flags, const DeviceInfo& dev,
+                       cudaStream_t s) {
+  GemvArgs g;
+  g.x = x;
+  g.a_scales = a_scales;
+  g.lds = lds;
+  g.b = b;
+  g.ldb = ldb;
+  g.scales = sc;
+  g.fmt = fmt;
+  g.act = act;
+  g.C = c;
+  g.N = int(N);
+  g.K = int(K);
+  g.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
+  g.out_f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
+  g.err = dev.err_word;
+  return cuda_status(launch_gemv(g, dev, s));
+}
+
 fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, const void* sc, int fmt, void* c,
                         int64_t ldc, int64_t M, int64_t N, int64_t K, uint32_t flags, cudaStream_t s) {
   DeviceInfo dev;
@@ -184,24 +206,7 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   if (st != FP8BLK_OK) return st;
   const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
   if (K == 0) return zero_output(c, ldc, M, N, f32 ? 4 : 2, s);
-  if (gemv_window(M, N, K, dev)) {
-    GemvArgs g;
-    g.x = x;
-    g.a_scales = nullptr;
-    g.lds = 0;
-    g.b = b;
-    g.ldb = ldb;
-    g.scales = sc;
-    g.fmt = fmt;
-    g.act = kGemvActBf16;
-    g.C = c;
-    g.N = int(N);
-    g.K = int(K);
-    g.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
-    g.out_f32 = f32;
-    g.err = dev.err_word;
-    return cuda_status(launch_gemv(g, dev, s));
-  }
+  if (gemv_window(M, N, K, dev)) return run_gemv(kGemvActBf16, x, nullptr, 0, b, ldb, sc, fmt, c, N, K, flags, dev, s);
   GemmW8A16Args p;
   p.scales = sc;
   p.fmt = fmt;
@@ -249,24 +254,8 @@ fp8blk_status run_w8a8(const void* a_e4m3, int64_t lda, const float* a_scales, i
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
   if (K == 0) return zero_output(c_bf16, ldc, M, N, f32 ? 4 : 2, s);
-  if (G == 0 && gemv_window(M, N, K, dev)) {
-    GemvArgs g;
-    g.x = a_e4m3;
-    g.a_scales = a_scales;
-    g.lds = lds;
-    g.b = b_e4m3;
-    g.ldb = ldb;
-    g.scales = b_scales;
-    g.fmt = 0;
-    g.act = kGemvActE4m3;
-    g.C = c_bf16;
-    g.N = int(N);
-    g.K = int(K);
-    g.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
-    g.out_f32 = f32;
-    g.err = dev.err_word;
-    return cuda_status(launch_gemv(g, dev, s));
-  }
+  if (G == 0 && gemv_window(M, N, K, dev))
+    return run_gemv(kGemvActE4m3, a_e4m3, a_scales, lds, b_e4m3, ldb, b_scales, 0, c_bf16, N, K, flags, dev, s);
   const int64_t b_rows = G > 0 ? G * N : N;
   GemmW8A8Args p;
   std::memset(&p.tmX, 0, sizeof(p.tmX));     // read only by the fused form
@@ -366,24 +355,8 @@ fp8blk_status fp8blk_linear_w8a8(const void* x_bf16, int64_t ldx, const void* b_
   if (st != FP8BLK_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return zero_output(c_bf16, ldc, M, N, f32 ? 4 : 2, s);
-  if (gemv_window(M, N, K, dev)) {
-    GemvArgs g;
-    g.x = x_bf16;
-    g.a_scales = nullptr;
-    g.lds = 0;
-    g.b = b_e4m3;
-    g.ldb = ldb;
-    g.scales = b_scales;
-    g.fmt = 0;
-    g.act = kGemvActQuant;
-    g.C = c_bf16;
-    g.N = int(N);
-    g.K = int(K);
-    g.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
-    g.out_f32 = f32;
-    g.err = dev.err_word;
-    return cuda_status(launch_gemv(g, dev, s));
-  }
+  if (gemv_window(M, N, K, dev))
+    return run_gemv(kGemvActQuant, x_bf16, nullptr, 0, b_e4m3, ldb, b_scales, 0, c_bf16, N, K, flags, dev, s);
   GemmW8A8Args p;
   std::memset(&p.tmA, 0, sizeof(p.tmA));     // not read by the fused form
   std::memset(&p.tmAs, 0, sizeof(p.tmAs));
