@@ -32,7 +32,7 @@
 //     "Exactness").
 //
 // Tiles run persistently; when the tile count cannot fill the GPU, K is split
-// over a 2..8-CTA cluster and the FP32 partial tiles are summed in rank order
+// over a 2..4-CTA cluster and the FP32 partial tiles are summed in rank order
 // through distributed shared memory by rank 0.
 #include <cuda_bf16.h>
 
@@ -279,7 +279,11 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
       int nt, mt;
       tile_coords(t, n_tiles, m_tiles, nt, mt);
       const int n = nt * BN + row;
-      const uint8_t* ue_row = ue + size_t(n / 32) * (K / 32);
+      // The warp's 32 rows share one UE8M0 scale row (n / 32): its four bytes
+      // per K block are loaded 32 K blocks at a time, one K block per lane,
+      // and handed out by shuffles, so no global load waits on the decode.
+      const uint32_t* ue_row = reinterpret_cast<const uint32_t*>(ue + size_t(n / 32) * (K / 32));
+      uint32_t e4_win = 0;
       for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
         const int s = it % Q::kStages;
         const uint32_t ph = (it / Q::kStages) & 1u;
@@ -288,7 +292,9 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
         // multipliers for the four 32-wide K groups of this block
         uint32_t mul[4];
         if (ue8m0) {
-          const uint32_t e4 = *reinterpret_cast<const uint32_t*>(ue_row + kb * 4);
+          const int wi = (kb - kb_begin) & 31;
+          if (wi == 0) e4_win = kb + lane < kb_end ? __ldg(ue_row + kb + lane) : 0u;
+          const uint32_t e4 = __shfl_sync(0xffffffffu, e4_win, wi);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const int e = int((e4 >> (8 * g)) & 0xFFu) - 127;
@@ -360,6 +366,7 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
       for (int kb = kb_begin; kb < kb_stop; ++kb, ++acc_it) {
         const int d = acc_it % Q::kDBufs;
         const uint32_t dph = (acc_it / Q::kDBufs) & 1u;
+        // (issued before the wait for the partial, which takes longer)
         const float sc = ue8m0 ? 1.f : __ldg(bs32 + size_t(nt) * kblocks + kb);
         const bool got = __all_sync(0xffffffffu, mbar_wait(&dfull[d], dph, abort_flag));
         if (!got) {
@@ -454,9 +461,13 @@ cudaError_t launch_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_
   const int tiles = n_tiles * m_tiles;
   const int kblocks = p.K / BK;
   const int slots = dev.num_sms * Q::kMinBlocks;
+  // K is split over at most 4 CTAs: with 16 tiles of K = 7168 at M = 64 or
+  // 128, 8-way splits took 20-21 us against 16 us for 4-way (the 8-rank
+  // reduction of 64 KB partial tiles costs more than the K blocks it saves).
+  constexpr int kSplitCap = 4;
   int split = 1;
   if (tiles * 2 <= slots) {
-    for (int s = kMaxSplitK; s >= 2; s >>= 1) {
+    for (int s = kSplitCap; s >= 2; s >>= 1) {
       if (tiles * s <= slots && kblocks >= 2 * s) {
         split = s;
         break;
