@@ -34,7 +34,7 @@
 // raster order so that concurrently running tiles share A and B panels in L2
 // ("Blockwise FP8 on Ada GPUs, part 2", "One tile doesn't fit all M": the
 // launch-order swizzle).  Problems with too few tiles to fill the GPU split K
-// over a thread-block cluster of 2..8 CTAs; the partial accumulators are
+// over a thread-block cluster of 2..4 CTAs; the partial accumulators are
 // summed through distributed shared memory in rank order (no global
 // workspace), and rank 0 writes C.
 //
@@ -619,9 +619,13 @@ cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStre
   const int n_tiles = p.N / BN;
   const int tiles = m_tiles * n_tiles;
   const int kblocks = p.K / BK;
+  // K is split over at most 4 CTAs: with 16 tiles of K = 7168 at M = 16 or
+  // 128, 8-way splits took 19 and 33 us against 12.4 and 16 us for 4-way
+  // (the 8-rank reduction costs more than the K blocks it saves).
+  constexpr int kSplitCap = 4;
   int split = 1;
   if (tiles * 2 <= dev.num_sms && p.row_group == nullptr) {
-    for (int s = kMaxSplitK; s >= 2; s >>= 1) {
+    for (int s = kSplitCap; s >= 2; s >>= 1) {
       if (tiles * s <= dev.num_sms && kblocks >= 2 * s) {
         split = s;
         break;
