@@ -138,7 +138,9 @@ def test_gemv_w8a16_ue8m0(lib, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(17, 256, 512), (32, 512, 1024), (33, 256, 256), (64, 384, 2048),
-                                   (100, 256, 512), (128, 512, 512), (129, 256, 1024), (512, 1024, 512)])
+                                   (100, 256, 512), (128, 512, 512), (129, 256, 1024), (512, 1024, 512),
+                                   (128, 512, 1152),      # K split over 4 CTAs with 9 K blocks: ranks of 2 and 3
+                                   (64, 256, 896)])       # K split over 2 CTAs with 7 K blocks
 @pytest.mark.parametrize("fmt", [0, 1])
 def test_gemm_w8a16(lib, M, N, K, fmt):
     x = synth.activations(M * 3 + K, M, K, outliers=True)

@@ -25,7 +25,9 @@ def gpu_quant_act(x_bits, lds_pad=0, ldx_pad=0):
 
 
 @pytest.mark.parametrize("M,K,outliers", [(16, 512, False), (1, 128, False), (3, 384, True), (17, 1024, True),
-                                          (129, 4096, True), (300, 256, False)])
+                                          (129, 4096, True), (300, 256, False),
+                                          (257, 640, True),      # TMA-fed kernel, one row past a 64-row tile
+                                          (4100, 384, True)])    # more tiles than CTAs, ragged last tile
 def test_quant_act_matches_oracle(lib, M, K, outliers):
     x = synth.activations(M * 7 + K, M, K, outliers=outliers)
     a, s, lds = gpu_quant_act(x, lds_pad=4, ldx_pad=64)
