@@ -92,6 +92,20 @@ def test_w8a8_full_size_sampled_rows(lib):
     assert_gemm_close(out[rows], O.gemm_w8a8_rows(a, As, b, Bs, rows), "w8a8 4096^3 sampled")
 
 
+def test_w8a8_prefill_size_sampled_rows(lib):
+    """A prefill workload at full size (M = 2048, N = 18432, K = 7168: 576
+    CTA-pair tiles, 7.6 rounds), checked on 16 sampled rows."""
+    M, N, K = 2048, 18432, 7168
+    a, As = O.quant_act_1x128(synth.activations(2, M, K))
+    # Weight codes and block scales drawn directly (quantising 132 M weights
+    # in float64 would dominate the test): uniform finite codes, scales 2^-12..2^-6.
+    b = synth.finite_e4m3_codes(2, (N, K))
+    Bs = np.exp2(np.random.default_rng(2).uniform(-12, -6, size=(N // 128, K // 128))).astype(np.float32)
+    out = gpu_w8a8(a, As, b, Bs)
+    rows = synth.sample_rows(2, M, 16)
+    assert_gemm_close(out[rows], O.gemm_w8a8_rows(a, As, b, Bs, rows), "w8a8 2048x18432x7168 sampled")
+
+
 def test_w8a8_one_hot_rows(lib):
     """Each A row holds a single 1.0 at column k0: C row = Bs * dec(B[:, k0])."""
     N, K = 256, 512
