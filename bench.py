@@ -617,6 +617,20 @@ def probe():
             t = best(fn)
             print(json.dumps({"probe": "hbm", "op": what, "mib": nbytes >> 20, "gb_s": round(moved / t / 1e9, 1)}))
         del a, b
+    # Per-kernel floor: a one-element kernel replayed 200 times in a CUDA graph.
+    t1 = torch.zeros(1, device=dev)
+    g = torch.cuda.CUDAGraph()
+    s_cap = torch.cuda.Stream()
+    s_cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s_cap):
+        t1.add_(1.0)
+    torch.cuda.current_stream().wait_stream(s_cap)
+    with torch.cuda.graph(g, stream=s_cap):
+        for _ in range(200):
+            t1.add_(1.0)
+    t = best(g.replay) / 200
+    print(json.dumps({"probe": "kernel floor", "op": "one-element kernel, 200 per CUDA graph", "us_per_kernel":
+                      round(t * 1e6, 2)}))
     n = HEAD_M * HEAD_K * 2
     h = [torch.empty(n, dtype=torch.uint8).pin_memory() for _ in range(2)]
     d = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(2)]
