@@ -56,6 +56,7 @@ EXPORTS = {
     "fp8blk_quant_weight": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "fp8blk_validate_weights": (_I32, [_P, _I64, _P, _I32, _I64, _I64, _P, _P]),
     "fp8blk_debug_decode_e4m3": (_I32, [_P, _I64, _I32, _P, _P]),
+    "fp8blk_debug_group_scale": (_I32, [_P, _I64, _P, _P, _P, _P]),
     "fp8blk_debug_wait_timeout": (_I32, [_I64, _P]),
     "fp8blk_query_constraints": (_I32, [_P]),
     "fp8blk_status_string": (ctypes.c_char_p, [_I32]),
@@ -226,6 +227,12 @@ def fp8blk_validate_weights(b, b_scales, fmt, dev_counts, stream=None):
     N, K = b.shape
     _check(_L().fp8blk_validate_weights(_ptr(b), _ld(b), _ptr(b_scales), int(fmt), N, K, _ptr(dev_counts),
                                        _stream(stream)), "fp8blk_validate_weights")
+
+
+def fp8blk_debug_group_scale(amax, s_out, divisor_out, recip_out, stream=None):
+    """Runs the quantisers' scale arithmetic on float32 group maxima (device)."""
+    _check(_L().fp8blk_debug_group_scale(_ptr(amax), amax.numel(), _ptr(s_out), _ptr(divisor_out), _ptr(recip_out),
+                                         _stream(stream)), "fp8blk_debug_group_scale")
 
 
 def fp8blk_debug_decode_e4m3(codes, exp_shift, out, stream=None):

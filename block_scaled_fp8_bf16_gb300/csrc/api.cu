@@ -462,6 +462,21 @@ fp8blk_status fp8blk_debug_decode_e4m3(const void* codes, int64_t n, int32_t exp
   return cuda_status(launch_debug_decode(codes, n, exp_shift, out_bf16, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8blk_status fp8blk_debug_group_scale(const float* amax, int64_t n, float* s_out, float* divisor_out,
+                                       float* recip_out, fp8blk_stream_t stream) {
+  if (n < 0 || n > kIntMax) return FP8BLK_ERR_INVALID_ARG;
+  if (n == 0) return FP8BLK_OK;
+  if (!amax || !s_out || !divisor_out || !recip_out) return FP8BLK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(amax) & 3u) != 0 || (reinterpret_cast<uintptr_t>(s_out) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(divisor_out) & 3u) != 0 || (reinterpret_cast<uintptr_t>(recip_out) & 3u) != 0)
+    return FP8BLK_ERR_MISALIGNED;
+  DeviceInfo dev;
+  fp8blk_status st = device_info(dev);
+  if (st != FP8BLK_OK) return st;
+  return cuda_status(
+      launch_debug_group_scale(amax, n, s_out, divisor_out, recip_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 fp8blk_status fp8blk_debug_wait_timeout(int64_t limit_ns, fp8blk_stream_t stream) {
   if (limit_ns < 1000 || limit_ns > 100000000) return FP8BLK_ERR_INVALID_ARG;
   DeviceInfo dev;

@@ -75,6 +75,7 @@ struct ValidateArgs {
 cudaError_t launch_validate(const ValidateArgs& p, const DeviceInfo& dev, cudaStream_t s);
 
 cudaError_t launch_debug_decode(const void* codes, int64_t n, int exp_shift, void* out, cudaStream_t s);
+cudaError_t launch_debug_group_scale(const float* amax, int64_t n, float* s, float* ds, float* y, cudaStream_t st);
 cudaError_t launch_debug_wait_timeout(int64_t limit_ns, int code, int* err, cudaStream_t s);
 
 // ------------------------------------------------------------------ W8A8

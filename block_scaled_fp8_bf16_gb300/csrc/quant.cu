@@ -372,6 +372,25 @@ cudaError_t launch_debug_wait_timeout(int64_t limit_ns, int code, int* err, cuda
   return cudaGetLastError();
 }
 
+// Runs the quantisers' scale arithmetic on n group maxima: s = group_scale,
+// and the divisor make_divisor(s) forms (scaled divisor and its reciprocal).
+__global__ void debug_group_scale_kernel(const float* __restrict__ amax, int64_t n, float* __restrict__ s_out,
+                                         float* __restrict__ ds_out, float* __restrict__ y_out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float s = group_scale(amax[i]);
+  const Divisor d = make_divisor(s);
+  s_out[i] = s;
+  ds_out[i] = d.s;
+  y_out[i] = d.y;
+}
+
+cudaError_t launch_debug_group_scale(const float* amax, int64_t n, float* s, float* ds, float* y, cudaStream_t st) {
+  const int grid = int((n + 255) / 256);
+  debug_group_scale_kernel<<<grid, 256, 0, st>>>(amax, n, s, ds, y);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_debug_decode(const void* codes, int64_t n, int exp_shift, void* out, cudaStream_t s) {
   const int64_t words = n / 4;
   const int grid = int((words + 255) / 256);

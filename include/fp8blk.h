@@ -316,6 +316,17 @@ FP8BLK_API fp8blk_status fp8blk_debug_decode_e4m3(const void* codes, int64_t n, 
                                        void* out_bf16, fp8blk_stream_t stream);
 
 /*
+ * Diagnostic: runs the activation quantisers' scale arithmetic on n group
+ * maxima (finite, >= 0): s_out[i] = the group scale amax / 448 (1 for a zero
+ * maximum), divisor_out[i] = s scaled by an exact power of two into
+ * [2^-60, 2^64], recip_out[i] = the reciprocal the quotients use.  All device
+ * float32 arrays of n elements, 4-byte aligned.
+ */
+FP8BLK_API fp8blk_status fp8blk_debug_group_scale(const float* amax, int64_t n, float* s_out,
+                                       float* divisor_out, float* recip_out,
+                                       fp8blk_stream_t stream);
+
+/*
  * Failure-detection check of the bounded waits (no counterpart in the pages;
  * it exercises the library's own error path).  Launches one warp that
  * initialises an mbarrier nobody arrives on and waits for it with the same

@@ -136,3 +136,28 @@ def test_quant_act_many_scales_across_the_exponent_range(lib):
     qa, qs = O.quant_act_1x128(x)
     assert np.array_equal(s[:, : x.shape[0]].view(np.uint32), qs.view(np.uint32))
     assert np.array_equal(a, qa)
+
+
+def test_group_scale_arithmetic_every_bf16_amax(lib):
+    """The quantisers' scale arithmetic on every finite non-negative bf16 group
+    maximum: s equals the correctly rounded amax / 448 (1 for zero), the
+    divisor is s times a power of two inside [2^-60, 2^64], and its reciprocal
+    is the correctly rounded 1 / divisor (float64 quotient rounded to float32,
+    which double rounding leaves exact)."""
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    bits = np.arange(0x0000, 0x7F80, dtype=np.uint16)
+    amax = O.bf16_bits_to_f64(bits).astype(np.float32)
+    n = amax.size
+    dev = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(3)]
+    fp8blk.fp8blk_debug_group_scale(torch.from_numpy(amax).cuda(), *dev)
+    torch.cuda.synchronize()
+    s, ds, y = (t.cpu().numpy() for t in dev)
+    s_ref = np.where(amax == 0, np.float32(1.0), O.fp32_div(amax, np.float32(448.0))).astype(np.float32)
+    bad = np.nonzero(s.view(np.uint32) != s_ref.view(np.uint32))[0]
+    assert bad.size == 0, f"scale differs for amax bits {bits[bad[:5]]}"
+    ratio = ds.astype(np.float64) / s.astype(np.float64)
+    assert np.all(np.log2(ratio) == np.round(np.log2(ratio)))
+    assert np.all((ds >= 2.0 ** -60) & (ds <= 2.0 ** 64))
+    y_ref = (1.0 / ds.astype(np.float64)).astype(np.float32)
+    bad = np.nonzero(y.view(np.uint32) != y_ref.view(np.uint32))[0]
+    assert bad.size == 0, f"reciprocal differs for amax bits {bits[bad[:5]]}"
