@@ -155,6 +155,12 @@ def test_quant_argument_errors(fp8blk):
     assert d(n=6) == 1
     assert d(e=8) == 1
     assert d(e=-15) == 1
+    g = lambda n=64, a=P, s=P, ds=P, y=P: lib.fp8blk_debug_group_scale(a, n, s, ds, y, None)
+    assert g(n=-1) == 1
+    assert g(n=0) == 0
+    assert g(y=None) == 1
+    assert g(a=None) == 1
+    assert g(s=P + 2) == 3
 
 
 def test_valid_call_without_gpu_reports_cuda_or_arch(fp8blk):
