@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
     const int sub = lane & 7;              // 16-column slice of the row
     const int rg = lane >> 3;              // row within the pass
     constexpr int kPasses = kFusedMaxM / (4 * Q::kQuantWarps);
-    constexpr int kNarrowM = 8;            // up to this many rows: one warp per row
+    constexpr int kNarrowM = 4;            // up to this many rows: one warp per row
     static_assert(kPasses % 2 == 0, "passes run in pairs");
     uint32_t it = 0;
     bool ok = true;

@@ -17,6 +17,8 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("M,N,K,dtype", [
     (1, 256, 512, torch.bfloat16),
     (16, 256, 512, torch.bfloat16),       # the tiny workload
+    (5, 384, 512, torch.bfloat16),        # few rows on the eight-lanes-per-row quantiser path
+    (4, 256, 1024, torch.float32),        # the one-warp-per-row quantiser path at its limit
     (32, 384, 1024, torch.bfloat16),
     (7, 4096, 4096, torch.bfloat16),      # K split over a cluster
     (1, 4096, 4096, torch.float32),       # one-token GEMV quantising its token
