@@ -67,6 +67,19 @@ def test_w8a8_two_weight_scales_per_256_columns(lib):
     assert_gemm_close(gpu_w8a8(a, As, b, Bs), O.gemm_w8a8(a, As, b, Bs), "w8a8 Bs slices")
 
 
+def test_w8a8_pair_path_weight_scales_per_slice(lib):
+    """The CTA-pair kernel (M = 1024, N = 2560: 40 tiles of 256 x 256, each
+    spanning two weight-scale slices) with weight scales that differ by up
+    to 10^6 between the two 128-column halves of a tile and between K
+    blocks: each half must take the scale of its own slice for every K
+    block."""
+    M, N, K = 1024, 2560, 512
+    a, As, b, Bs = w8a8_inputs(11, M, N, K)
+    f = np.array([1.0, 1000.0, 1e-3, 7.0, 0.5], dtype=np.float32)
+    Bs = Bs * f[(np.arange(N // 128)[:, None] + 2 * np.arange(K // 128)[None, :]) % len(f)]
+    assert_gemm_close(gpu_w8a8(a, As, b, Bs), O.gemm_w8a8(a, As, b, Bs), "w8a8 pair Bs slices")
+
+
 def test_w8a8_special_rows(lib):
     """A zero row, an outlier row and a row of +-448 codes."""
     M, N, K = 8, 256, 1024
