@@ -524,6 +524,10 @@ fp8blk_status fp8blk_device_error(int32_t* out_code, int32_t clear) {
   DeviceInfo dev;
   fp8blk_status st = device_info(dev);
   if (st != FP8BLK_OK) return st;
+  // Every stream of the device, non-blocking ones included, must have
+  // finished before the word is read: a kernel still running on such a
+  // stream could record a timeout after the read, or after the clear.
+  if (cudaDeviceSynchronize() != cudaSuccess) return FP8BLK_ERR_CUDA;
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_err_word, sizeof(int)) != cudaSuccess) return FP8BLK_ERR_CUDA;
   *out_code = v;

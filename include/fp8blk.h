@@ -348,10 +348,14 @@ FP8BLK_API fp8blk_status fp8blk_query_constraints(fp8blk_constraints* out);
 FP8BLK_API const char* fp8blk_status_string(fp8blk_status status);
 
 /*
- * Reads the current device's error word (synchronises the device).
+ * Reads the current device's error word.  It first waits for all work on
+ * the device to finish (cudaDeviceSynchronize: every stream, non-blocking
+ * ones included), so a kernel that gave up on a wait is always seen, and a
+ * clear cannot race a kernel that records a timeout later.
  * *out_code receives the raw word (0 = no error; otherwise an internal code
  * naming the wait that expired).  Returns FP8BLK_ERR_TIMEOUT when the word
- * is set, FP8BLK_OK when clear.  clear != 0 resets the word to 0.
+ * is set, FP8BLK_OK when clear, FP8BLK_ERR_CUDA when the synchronisation or
+ * the read fails.  clear != 0 resets the word to 0.
  */
 FP8BLK_API fp8blk_status fp8blk_device_error(int32_t* out_code, int32_t clear);
 

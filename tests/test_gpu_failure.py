@@ -42,6 +42,20 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert fp8blk.fp8blk_device_error() == 0
 
 
+def test_timeout_on_a_non_blocking_stream_is_seen_without_a_sync():
+    """The timeout kernel runs on a non-blocking stream (which the legacy
+    default stream does not wait for); fp8blk_device_error must still see
+    the code without any synchronisation by the caller."""
+    import torch
+
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    fp8blk.fp8blk_device_error(clear=True)
+    side = torch.cuda.Stream()
+    fp8blk.fp8blk_debug_wait_timeout(20_000_000, side)   # 20 ms: still waiting when the read is issued
+    assert fp8blk.fp8blk_device_error(clear=True) == fp8blk.DIAG_TIMEOUT_CODE
+    assert fp8blk.fp8blk_device_error() == 0
+
+
 def test_timeout_status_maps_to_err_timeout():
     import ctypes
 
