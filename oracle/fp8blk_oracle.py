@@ -42,6 +42,16 @@ tests/test_oracle_gemm.py):
                          equals the single-weight product with its group's
                          weights (int64 brute force on tiny inputs); row-block
                          permutation invariance; padding rows stay untouched.
+  act_exponent_ue8m0     pinned: minimality checked by exact comparisons on
+                         every finite bf16 magnitude; page-independent special
+                         values (448 -> 0, 450 -> 1, 224 -> -1, 1 -> -8, 0 and
+                         subnormals -> -127).
+  quant_act_1x32_ue8m0   pinned: torch's float8_e4m3fn cast of x * 2^-e on
+                         exhaustive bf16 groups; reconstruction within half an
+                         e4m3 ulp; the group maximum lands in (224, 448].
+  gemm_w8a8_ue8m0        pinned: Fraction brute force on tiny inputs; reduces
+                         to gemm_w8a8 when the exponents are constant over
+                         1x128 / 128x128 blocks; one-hot rows.
   End-to-end output numbers are "parity unpinned" against the pages: no page
   prints a per-element worked example of the product.
 """
@@ -56,6 +66,8 @@ __all__ = [
     "gemm_w8a8", "gemm_w8a16_f32scale", "gemm_w8a16_ue8m0", "gemm_w8a8_grouped",
     "gemm_w8a8_rows", "gemm_w8a16_f32scale_rows", "gemm_w8a16_ue8m0_rows",
     "UE8M0_EMIN", "UE8M0_EMAX", "UE8M0_BIAS",
+    "ACT_EXP_MIN", "ACT_EXP_MAX", "act_exponent_ue8m0", "quant_act_1x32_ue8m0",
+    "gemm_w8a8_ue8m0", "gemm_w8a8_ue8m0_rows",
 ]
 
 # Largest finite e4m3 magnitude and the two NaN codes of the finite-only
@@ -72,6 +84,15 @@ UE8M0_EMAX = 7
 
 QBLOCK = 128          # K width of one scale block [P1 "The starting point"]
 UE8M0_BLOCK = 32      # side of one UE8M0 block [P3 "How it works"]
+
+# W8A8 in the 32x32 UE8M0 format needs power-of-two activation scales too,
+# one per token per 32 values of K (a 32x32 weight block meets 1x32
+# activation groups).  The pages fix neither the rule nor the range; the
+# reading: the smallest power of two 2^e with 448 * 2^e >= amax (no element
+# saturates), e clamped to the byte range of a UE8M0 scale [-127, 127]
+# (byte 255 is NaN in E8M0), and amax == 0 takes the clamp, e = -127.
+ACT_EXP_MIN = -127
+ACT_EXP_MAX = 127
 
 
 # ---------------------------------------------------------------------------
@@ -340,3 +361,76 @@ def gemm_w8a16_ue8m0_rows(x_bf16_bits, b_codes, b_scale_bytes, rows=None) -> np.
 
 def gemm_w8a16_ue8m0(x_bf16_bits, b_codes, b_scale_bytes) -> np.ndarray:
     return gemm_w8a16_ue8m0_rows(x_bf16_bits, b_codes, b_scale_bytes, None)
+
+
+# ---------------------------------------------------------------------------
+# W8A8 in the 32x32 UE8M0 format
+# ---------------------------------------------------------------------------
+
+def act_exponent_ue8m0(amax) -> np.ndarray:
+    """Exponent e of a 1x32 activation group's power-of-two scale: the
+    smallest integer with 448 * 2^e >= amax, clamped to [-127, 127]
+    (reading; see ACT_EXP_MIN).  Written out as that definition: start from
+    the float estimate ceil(log2(amax / 448)) and step to the smallest
+    integer that passes the exact test 448 * 2^e >= amax (both sides exact
+    in float64).  amax == 0 gives the clamp, -127."""
+    a = np.asarray(amax, dtype=np.float64)
+    out = np.empty(a.shape, dtype=np.int64)
+    for idx, v in np.ndenumerate(a):
+        if v == 0.0:
+            out[idx] = ACT_EXP_MIN
+            continue
+        e = int(np.ceil(np.log2(v / E4M3_MAX)))
+        while np.ldexp(E4M3_MAX, e) < v:            # too small: 448 * 2^e must reach amax
+            e += 1
+        while np.ldexp(E4M3_MAX, e - 1) >= v:       # not the smallest
+            e -= 1
+        out[idx] = min(max(e, ACT_EXP_MIN), ACT_EXP_MAX)
+    return out
+
+
+def quant_act_1x32_ue8m0(x_bf16_bits: np.ndarray):
+    """Per-token 1x32 activation quantisation with UE8M0 (power-of-two)
+    scales, for W8A8 in the 32x32 UE8M0 weight format ("SM70 FP8 block-32
+    kernels", "How it works": one power of two per 32x32 block; "perf
+    (ArcKernels)", "Cheap checks done first": the VEC32_UE8M0 scale modes).
+
+    x: bf16 bits [M, K], K % 32 == 0.  Per group of 32: e from
+    act_exponent_ue8m0(max |x|), q = e4m3(x * 2^-e) (nearest, ties to even;
+    x * 2^-e is exact and never above 448, so no code saturates).
+    Returns (codes uint8 [M, K], exponent bytes uint8 [K/32, M] = e + 127,
+    M contiguous like the fp32 activation scales).
+    """
+    x = np.asarray(x_bf16_bits, dtype=np.uint16)
+    M, K = x.shape
+    assert K % UE8M0_BLOCK == 0
+    xv = bf16_bits_to_f64(x).reshape(M, K // UE8M0_BLOCK, UE8M0_BLOCK)
+    e = act_exponent_ue8m0(np.max(np.abs(xv), axis=-1))           # [M, K/32]
+    q = e4m3_encode(xv * np.exp2(-e.astype(np.float64))[..., None])
+    return q.reshape(M, K), np.ascontiguousarray((e + UE8M0_BIAS).astype(np.uint8).T)
+
+
+def gemm_w8a8_ue8m0_rows(a_codes, a_exp_bytes, b_codes, b_exp_bytes, rows=None) -> np.ndarray:
+    """W8A8 product in the 32x32 UE8M0 format, float64:
+
+        C[m, n] = sum_k dec(A[m, k]) 2^(ea[k/32, m] - 127) dec(B[n, k]) 2^(eb[n/32, k/32] - 127)
+
+    ("SM70 FP8 block-32 kernels", "How it works": the weight's power of two
+    per 32x32 block; the activation's per 1x32 group).  a_exp_bytes
+    [K/32, M] (M contiguous), b_exp_bytes [N/32, K/32].
+    """
+    A = np.asarray(a_codes)
+    ea = np.asarray(a_exp_bytes)
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        A = A[rows]
+        ea = ea[:, rows]
+    Ad = e4m3_decode(A) * np.repeat(ue8m0_value(ea).T, UE8M0_BLOCK, axis=1)
+    Bd = e4m3_decode(b_codes)
+    sb = ue8m0_value(b_exp_bytes)
+    Bd = Bd * np.repeat(np.repeat(sb, UE8M0_BLOCK, axis=0), UE8M0_BLOCK, axis=1)
+    return Ad @ Bd.T
+
+
+def gemm_w8a8_ue8m0(a_codes, a_exp_bytes, b_codes, b_exp_bytes) -> np.ndarray:
+    return gemm_w8a8_ue8m0_rows(a_codes, a_exp_bytes, b_codes, b_exp_bytes, None)
