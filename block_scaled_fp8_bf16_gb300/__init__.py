@@ -51,6 +51,8 @@ EXPORTS = {
     "fp8blk_linear_w8a8": (_I32, [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_gemm_w8a8_grouped": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _I64, _U32,
                                          _P]),
+    "fp8blk_quant_act_ue8m0": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
+    "fp8blk_gemm_w8a8_ue8m0": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_gemm_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_gemv_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_quant_weight": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P]),
@@ -157,6 +159,33 @@ def fp8blk_quant_act(x, a, a_scales, stream=None):
     M, K = x.shape
     _check(_L().fp8blk_quant_act(_ptr(x), M, K, _ld(x), _ptr(a), _ld(a), _ptr(a_scales), _ld(a_scales),
                                 _stream(stream)), "fp8blk_quant_act")
+
+
+def fp8blk_quant_act_ue8m0(x, a, a_exps, stream=None):
+    """x [M, K] bf16 -> a [M, K] e4m3 (uint8 view), a_exps [K/32, lde] uint8
+    (one power-of-two exponent byte per token per 32 values)."""
+    import torch
+    _expect(x, (torch.bfloat16,), "x")
+    _expect(a_exps, (torch.uint8,), "a_exps")
+    a = _bytes_tensor(a)
+    M, K = x.shape
+    _check(_L().fp8blk_quant_act_ue8m0(_ptr(x), M, K, _ld(x), _ptr(a), _ld(a), _ptr(a_exps), _ld(a_exps),
+                                      _stream(stream)), "fp8blk_quant_act_ue8m0")
+
+
+def fp8blk_gemm_w8a8_ue8m0(a, a_exps, b, b_exps, c, stream=None, flags=0):
+    """C[M, N] (bf16, or float32 when c is float32) = a[M, K] e4m3 x b[N, K] e4m3
+    with 1x32 activation and 32x32 weight UE8M0 exponents, on the tensor
+    cores' block scaling."""
+    import torch
+    _expect(a_exps, (torch.uint8,), "a_exps")
+    _expect(b_exps, (torch.uint8,), "b_exps")
+    a, b = _bytes_tensor(a), _bytes_tensor(b)
+    M, K = a.shape
+    N = b.shape[0]
+    _check(_L().fp8blk_gemm_w8a8_ue8m0(_ptr(a), _ld(a), _ptr(a_exps), _ld(a_exps), _ptr(b), _ld(b), _ptr(b_exps),
+                                      _ptr(c), _ld(c), M, N, K, _out_flags(c, flags), _stream(stream)),
+           "fp8blk_gemm_w8a8_ue8m0")
 
 
 def fp8blk_gemm_w8a8(a, a_scales, b, b_scales, c, stream=None, flags=0):
@@ -278,6 +307,29 @@ def quant_act(x, stream=None):
     s = torch.empty((K // 128, act_scales_pitch(M)), dtype=torch.float32, device=x.device)
     fp8blk_quant_act(x, a, s, stream)
     return a, s
+
+
+def act_exps_pitch(M: int) -> int:
+    """Row pitch (bytes) of the [K/32, lde] activation exponent array: M
+    rounded up to 16."""
+    return (M + 15) // 16 * 16
+
+
+def quant_act_ue8m0(x, stream=None):
+    import torch
+    M, K = x.shape
+    a = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    e = torch.empty((K // 32, act_exps_pitch(M)), dtype=torch.uint8, device=x.device)
+    fp8blk_quant_act_ue8m0(x, a, e, stream)
+    return a, e
+
+
+def gemm_w8a8_ue8m0(a, a_exps, b, b_exps, out=None, stream=None, flags=0, out_dtype=None):
+    import torch
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[0]), dtype=out_dtype or torch.bfloat16, device=a.device)
+    fp8blk_gemm_w8a8_ue8m0(a, a_exps, b, b_exps, out, stream, flags)
+    return out
 
 
 def quant_weight(w, stream=None):

@@ -20,8 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libfp8blk.so")
-SOURCES = ["api.cu", "quant.cu", "gemm_w8a8.cu", "gemm_w8a8_pair.cu", "gemm_w8a16.cu", "gemm_w8a16_decode.cu",
-           "gemv.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm_w8a8.cu", "gemm_w8a8_pair.cu", "gemm_w8a8_mx.cu", "gemm_w8a16.cu",
+           "gemm_w8a16_decode.cu", "gemv.cu"]
 HEADERS = ["ptx.cuh", "decode.cuh", "quant.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -381,6 +381,65 @@ fp8blk_status fp8blk_linear_w8a8(const void* x_bf16, int64_t ldx, const void* b_
   return cuda_status(launch_gemm_w8a8(p, dev, s));
 }
 
+fp8blk_status fp8blk_quant_act_ue8m0(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* a_e4m3,
+                                     int64_t lda, uint8_t* a_exps, int64_t lde, fp8blk_stream_t stream) {
+  if (M < 0 || K < 0) return FP8BLK_ERR_INVALID_ARG;
+  if (K % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || K == 0) return FP8BLK_OK;
+  if (!x_bf16 || !a_e4m3 || !a_exps) return FP8BLK_ERR_INVALID_ARG;
+  if (ldx < K || lda < K || lde < M) return FP8BLK_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(a_e4m3) || !aligned16(a_exps)) return FP8BLK_ERR_MISALIGNED;
+  if ((ldx * 2) % 16 != 0 || lda % 16 != 0 || lde % 16 != 0) return FP8BLK_ERR_MISALIGNED;
+  DeviceInfo dev;
+  fp8blk_status st = device_info(dev);
+  if (st != FP8BLK_OK) return st;
+  QuantActUe8m0Args p{x_bf16, ldx, M, K, a_e4m3, lda, a_exps, lde};
+  return cuda_status(launch_quant_act_ue8m0(p, dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fp8blk_status fp8blk_gemm_w8a8_ue8m0(const void* a_e4m3, int64_t lda, const uint8_t* a_exps, int64_t lde,
+                                     const void* b_e4m3, int64_t ldb, const uint8_t* b_exps, void* c, int64_t ldc,
+                                     int64_t M, int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || (flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
+  if (M > kIntMax || N > kIntMax || K > kIntMax) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return FP8BLK_OK;
+  if (!c) return FP8BLK_ERR_INVALID_ARG;
+  if (K > 0 && (!a_e4m3 || !a_exps || !b_e4m3 || !b_exps)) return FP8BLK_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldc < N || lde < M) return FP8BLK_ERR_INVALID_ARG;
+  if ((a_e4m3 && !aligned16(a_e4m3)) || (a_exps && !aligned16(a_exps)) || (b_e4m3 && !aligned16(b_e4m3)) ||
+      (b_exps && !aligned16(b_exps)) || !aligned16(c))
+    return FP8BLK_ERR_MISALIGNED;
+  const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
+  if (lda % 16 != 0 || ldb % 16 != 0 || (ldc * (f32 ? 4 : 2)) % 16 != 0 || lde % 16 != 0)
+    return FP8BLK_ERR_MISALIGNED;
+  DeviceInfo dev;
+  fp8blk_status st = device_info(dev);
+  if (st != FP8BLK_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(c, ldc, M, N, f32 ? 4 : 2, s);
+  GemmW8A8MxArgs p;
+  st = make_map(p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_e4m3, uint64_t(K), uint64_t(M), uint64_t(lda), 128, 128);
+  if (st != FP8BLK_OK) return st;
+  st = make_map(p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_e4m3, uint64_t(K), uint64_t(N), uint64_t(ldb), 128, 128);
+  if (st != FP8BLK_OK) return st;
+  if (f32)
+    st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, uint64_t(N), uint64_t(M), uint64_t(ldc) * 4, 32, 32);
+  else
+    st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c, uint64_t(N), uint64_t(M), uint64_t(ldc) * 2, 64, 32);
+  if (st != FP8BLK_OK) return st;
+  p.ea = a_exps;
+  p.lde = lde;
+  p.eb = b_exps;
+  p.M = int(M);
+  p.N = int(N);
+  p.K = int(K);
+  p.pdl = (flags & FP8BLK_FLAG_PDL) != 0;
+  p.out_f32 = f32;
+  p.err = dev.err_word;
+  return cuda_status(launch_gemm_w8a8_mx(p, dev, s));
+}
+
 fp8blk_status fp8blk_gemm_w8a8_grouped(const void* a_e4m3, int64_t lda, const float* a_scales, int64_t lds,
                                        const void* b_e4m3, int64_t ldb, const float* b_scales,
                                        const int32_t* row_group, int64_t G, void* c_bf16, int64_t ldc, int64_t M,

@@ -17,6 +17,7 @@ enum DeviceErr : int {
   kDevErrW8A16Decode = 0x300,
   kDevErrQuant = 0x400,
   kDevErrGemv = 0x500,
+  kDevErrW8A8Mx = 0x600,
 };
 enum WaitSite : int {
   kSiteProducerEmpty = 1,
@@ -105,6 +106,34 @@ cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaS
 // CTA-pair kernel (256 x 256 tiles); chosen by launch_gemm_w8a8 for large problems.
 int w8a8_pair_tiles(int M, int N);
 cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t s);
+
+// ------------------------------------------------------------------ W8A8, 32x32 UE8M0 format
+// Activation quantiser with power-of-two 1x32 scales (exponent bytes
+// [K/32][lde], M contiguous) and the block-scaled tensor-core product.
+struct QuantActUe8m0Args {
+  const void* x;      // bf16 [M, K] pitch ldx
+  int64_t ldx;
+  int64_t M, K;
+  void* a;            // e4m3 [M, K] pitch lda
+  int64_t lda;
+  uint8_t* ex;        // exponent bytes [K/32][lde]
+  int64_t lde;
+};
+cudaError_t launch_quant_act_ue8m0(const QuantActUe8m0Args& p, const DeviceInfo& dev, cudaStream_t s);
+
+struct GemmW8A8MxArgs {
+  CUtensorMap tmA;    // e4m3 [M, K], box {128 (K), 128 (M)}, 128B swizzle
+  CUtensorMap tmB;    // e4m3 [N, K], box {128 (K), 128 (N)}, 128B swizzle
+  CUtensorMap tmC;    // C [M, N], box {128 bytes of N, 32 (M)}, 128B swizzle
+  const uint8_t* ea;  // activation exponent bytes [K/32][lde]
+  int64_t lde;
+  const uint8_t* eb;  // weight exponent bytes [N/32][K/32]
+  int M, N, K;
+  bool pdl;
+  bool out_f32;
+  int* err;
+};
+cudaError_t launch_gemm_w8a8_mx(const GemmW8A8MxArgs& p, const DeviceInfo& dev, cudaStream_t s);
 
 // ------------------------------------------------------------------ W8A16
 struct GemmW8A16Args {

@@ -230,6 +230,54 @@ FP8BLK_API fp8blk_status fp8blk_gemm_w8a8_grouped(const void* a_e4m3, int64_t ld
                                uint32_t flags, fp8blk_stream_t stream);
 
 /*
+ * Per-token activation quantisation for W8A8 in the 32x32 UE8M0 weight
+ * format: one power-of-two scale per token per 32 values of K, so that each
+ * 1x32 activation slice meets one 32x32 weight block ("SM70 FP8 block-32
+ * kernels (PLI Labs)", "How it works": power-of-two scales per 32x32 block).
+ * For each group of 32: e = the smallest integer with 448 * 2^e >= max|x|
+ * (no code saturates), clamped to [-127, 126]; max|x| == 0 gives -127;
+ * q = e4m3(x * 2^-e), round to nearest even (x * 2^-e is exact).  The pages
+ * do not state how activation exponents are chosen; this is the reading.
+ *
+ *  x_bf16   [M, K] bf16, row pitch ldx elements (ldx*2 % 16 == 0).
+ *  a_e4m3   [M, K] e4m3 out, row pitch lda bytes (lda % 16 == 0).
+ *  a_exps   [K/32][lde] uint8 out, byte = e + 127, M contiguous;
+ *           lde >= M, lde % 16 == 0.
+ *  K % 128 == 0 (the product consumes 128-wide K blocks), M >= 0 (0: no-op).
+ *  All pointers 16-byte aligned.  Asynchronous on stream.
+ */
+FP8BLK_API fp8blk_status fp8blk_quant_act_ue8m0(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                               void* a_e4m3, int64_t lda, uint8_t* a_exps, int64_t lde,
+                               fp8blk_stream_t stream);
+
+/*
+ * W8A8 GEMM in the 32x32 UE8M0 format on the tensor cores' block scaling
+ * (tcgen05.mma kind::mxf8f6f4 with one UE8M0 scale per 32 values of K on
+ * each side; "perf(ArcKernels) ...", "Cheap checks done first" names these
+ * VEC32_UE8M0 modes): every K = 32 slice's product is scaled by
+ * 2^(ea - 127) * 2^(eb - 127) inside the MMA and accumulated in FP32, with
+ * no software promotion.
+ *
+ *   C[m, n] = sum_k A[m, k] 2^(ea[k/32][m] - 127) * B[n, k] 2^(eb[n/32][k/32] - 127)
+ *
+ *  a_e4m3, lda, a_exps, lde   as written by fp8blk_quant_act_ue8m0.
+ *  b_e4m3   [N, K] e4m3 weights, K contiguous, row pitch ldb bytes.
+ *  b_exps   [N/32][K/32] uint8 weight exponent bytes (the UE8M0 format of
+ *           fp8blk_gemm_w8a16), packed.
+ *  c        [M, N] bf16 out (round to nearest even), row pitch ldc
+ *           elements; float32 with FP8BLK_FLAG_OUT_F32.
+ *  N % 128 == 0, K % 128 == 0, M >= 0 (0: no-op), K == 0 zero-fills C.
+ *  flags    FP8BLK_FLAG_PDL, FP8BLK_FLAG_OUT_F32.
+ *  Weight codes are assumed finite and exponent bytes below 255 (the UE8M0
+ *  NaN); fp8blk_validate_weights checks the stricter [-14, 7] window.
+ */
+FP8BLK_API fp8blk_status fp8blk_gemm_w8a8_ue8m0(const void* a_e4m3, int64_t lda,
+                               const uint8_t* a_exps, int64_t lde,
+                               const void* b_e4m3, int64_t ldb, const uint8_t* b_exps,
+                               void* c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                               uint32_t flags, fp8blk_stream_t stream);
+
+/*
  * W8A16 GEMM: bf16 activations, e4m3 weights decoded to bf16 in registers by
  * integer operations, bf16 tensor-core products with FP32 accumulation
  * ("FP8 / NVFP4 weight-only inference on the RTX 3090 loses nothing",

@@ -208,3 +208,33 @@ def test_fused_linear_argument_errors(fp8blk):
     assert f(x=None) == 1
     assert f(ldx=516) == 3             # bf16 rows of x must be 16-byte multiples
     assert f(M=0) == 0                 # no-op, no device needed
+
+
+def test_ue8m0_w8a8_argument_errors(fp8blk):
+    L = fp8blk._L()
+    P = ctypes.c_void_p(16 * 1024)
+
+    def q(M=16, K=512, ldx=512, lda=512, lde=16, x=P, e=P):
+        return L.fp8blk_quant_act_ue8m0(x, M, K, ldx, P, lda, e, lde, None)
+
+    assert q(M=-1) == 1
+    assert q(K=96) == 2                 # K % 128
+    assert q(M=0) == 0                  # no-op
+    assert q(e=None) == 1
+    assert q(lde=8) == 1                # lde < M
+    assert q(lde=24) == 3               # exponent rows must be 16-byte multiples
+    assert q(x=ctypes.c_void_p(16 * 1024 + 8)) == 3
+    assert q(ldx=516) == 3
+
+    def g(M=16, N=256, K=512, lda=512, lde=16, ldb=512, ldc=256, flags=0, ea=P, eb=P, c=P):
+        return L.fp8blk_gemm_w8a8_ue8m0(P, lda, ea, lde, P, ldb, eb, c, ldc, M, N, K, flags, None)
+
+    assert g(N=96) == 2 and g(K=96) == 2
+    assert g(M=-1) == 1 and g(flags=4) == 1
+    assert g(M=0) == 0 and g(N=0) == 0  # no-ops, no device needed
+    assert g(ea=None) == 1 and g(eb=None) == 1 and g(c=None) == 1
+    assert g(lde=8) == 1                # lde < M
+    assert g(lde=24) == 3
+    assert g(eb=ctypes.c_void_p(16 * 1024 + 4)) == 3
+    assert g(ldc=260) == 3              # bf16 rows need ldc * 2 % 16 == 0
+    assert g(ldc=260, flags=2) != 3     # float32 rows of that pitch are fine
