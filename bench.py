@@ -428,7 +428,7 @@ def reference_arm(args, world, rank):
 
 def sweep(out_path, kinds=None):
     """Times every workload shape with CUDA-graph replays over rotated copies
-    (kinds: optional subset of "w8a8", "grouped", "w8a16")."""
+    (kinds: optional subset of "w8a8", "grouped", "w8a16", "linear", "mx")."""
     import torch
 
     import block_scaled_fp8_bf16_gb300 as fp8blk
@@ -559,6 +559,51 @@ def sweep(out_path, kinds=None):
                    2.0 * M * N * K, byt, pk["bf16"])
         del sets
         torch.cuda.empty_cache()
+    # Decode-size W8A8 linear: the fused quantising kernel against
+    # fp8blk_quant_act + fp8blk_gemm_w8a8 (the rows the binding's choice
+    # between the two forms is taken from).
+    linear = [(M, N, K) for M in (2, 4, 8, 16, 32) for N, K in ((4096, 4096), (7168, 2048), (2048, 7168), (256, 512))]
+    if kinds is not None and "linear" not in kinds:
+        linear = []
+    for M, N, K in linear:
+        per = M * K * 3 + N * K + M * N * 2
+        R = _rot_copies(per, l2, cap=64)
+        sets = build_w8a8_set(M, N, K, R, outliers=False)
+        byt = N * K + (N // 128) * (K // 128) * 4 + 2 * M * K + 2 * M * N
+        for flags, tag in ((0, ""), (PDL, "_pdl")):
+            two = [lambda s=s, f=flags: (fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"]),
+                                         fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"], flags=f))
+                   for s in sets]
+            record("w8a8_linear" + tag, M, N, K, graph_time(two), 2.0 * M * N * K, byt, fp8_peak)
+            fused = [lambda s=s, f=flags: fp8blk.fp8blk_linear_w8a8(s["x"], s["b"], s["bs"], s["c"], flags=f)
+                     for s in sets]
+            record("w8a8_linear_fused" + tag, M, N, K, graph_time(fused), 2.0 * M * N * K, byt, fp8_peak)
+        del sets
+        torch.cuda.empty_cache()
+    # W8A8 in the 32x32 UE8M0 format (block-scaled tensor cores): the product
+    # alone and quantiser + product.
+    mx = [(M, N, K) for M in (128, 512, 4096, 8192) for N, K in ((2048, 7168), (7168, 2048))]
+    if kinds is not None and "mx" not in kinds:
+        mx = []
+    for M, N, K in mx:
+        per = M * K * 3 + N * K + M * N * 2
+        R = _rot_copies(per, l2, cap=32)
+        x = tg.activations(1, M, K)
+        b, eb = tg.ue8m0_weights(1, N, K)
+        sets = []
+        for _ in range(R):
+            a, e = fp8blk.quant_act_ue8m0(x)
+            sets.append({"x": x.clone(), "a": a, "e": e, "b": b.clone(), "eb": eb.clone(),
+                         "c": torch.empty((M, N), dtype=torch.bfloat16, device="cuda")})
+        byt = M * K + (K // 32) * M + N * K + (N // 32) * (K // 32) + 2 * M * N
+        calls = [lambda s=s: fp8blk.fp8blk_gemm_w8a8_ue8m0(s["a"], s["e"], s["b"], s["eb"], s["c"]) for s in sets]
+        record("w8a8_ue8m0_gemm", M, N, K, graph_time(calls), 2.0 * M * N * K, byt, fp8_peak)
+        calls = [lambda s=s: (fp8blk.fp8blk_quant_act_ue8m0(s["x"], s["a"], s["e"]),
+                              fp8blk.fp8blk_gemm_w8a8_ue8m0(s["a"], s["e"], s["b"], s["eb"], s["c"],
+                                                            flags=PDL)) for s in sets]
+        record("w8a8_ue8m0_linear_pdl", M, N, K, graph_time(calls), 2.0 * M * N * K, byt + 2 * M * K, fp8_peak)
+        del sets
+        torch.cuda.empty_cache()
     with open(out_path, "w") as f:
         json.dump({"peaks": pk, "fp8_peak": fp8_peak, "rows": rows}, f, indent=1)
 
@@ -567,7 +612,9 @@ def sweep(out_path, kinds=None):
 
 def run_case(spec: str, iters: int):
     """Runs one kernel configuration `iters` times, untimed (for ncu captures).
-    spec: w8a8:M,N,K | quant:M,K | w8a16:M,N,K,fmt"""
+    spec: w8a8:M,N,K | quant:M,K | w8a16:M,N,K,fmt | linear:M,N,K (fused quantising
+    W8A8, M <= 32) | grouped:G,rows_per_group,N,K | mx:M,N,K (UE8M0 W8A8:
+    quantiser + block-scaled product)"""
     import torch
 
     import block_scaled_fp8_bf16_gb300 as fp8blk
@@ -584,6 +631,33 @@ def run_case(spec: str, iters: int):
             fp8blk.fp8blk_quant_act(s["x"], s["a"], s["s"])
             if kind == "w8a8":
                 fp8blk.fp8blk_gemm_w8a8(s["a"], s["s"], s["b"], s["bs"], s["c"])
+    elif kind == "linear":
+        M, N, K = v
+        x = tg.activations(1, M, K)
+        b, bs = fp8blk.quant_weight(tg.weights_bf16(1, N, K))
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        for _ in range(iters):
+            fp8blk.fp8blk_linear_w8a8(x, b, bs, c)
+    elif kind == "grouped":
+        G, rows_per_group, N, K = v
+        M = G * rows_per_group
+        a, sc = fp8blk.quant_act(tg.activations(1, M, K))
+        ws = [fp8blk.quant_weight(tg.weights_bf16(1 + e, N, K)) for e in range(G)]
+        b = torch.stack([w[0] for w in ws])
+        bs = torch.stack([w[1] for w in ws])
+        rg = torch.arange(G, dtype=torch.int32, device="cuda").repeat_interleave(rows_per_group)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        for _ in range(iters):
+            fp8blk.fp8blk_gemm_w8a8_grouped(a, sc, b, bs, rg, c)
+    elif kind == "mx":
+        M, N, K = v
+        x = tg.activations(1, M, K)
+        b, eb = tg.ue8m0_weights(1, N, K)
+        a, e = fp8blk.quant_act_ue8m0(x)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        for _ in range(iters):
+            fp8blk.fp8blk_quant_act_ue8m0(x, a, e)
+            fp8blk.fp8blk_gemm_w8a8_ue8m0(a, e, b, eb, c)
     elif kind == "w8a16":
         M, N, K, fmt = v
         x = tg.activations(1, M, K)
@@ -685,7 +759,8 @@ def main():
                     help="comma list restricting --sweep to some of: w8a8, grouped, w8a16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None, help="run one configuration untimed (w8a8:M,N,K | quant:M,K | "
-                                                  "w8a16:M,N,K,fmt) for profiling")
+                    "linear:M,N,K | grouped:G,rows,N,K | mx:M,N,K | "
+                    "w8a16:M,N,K,fmt) for profiling")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--probe", action="store_true",
                     help="print device-memory and host-link rates (torch operations only) and exit")

@@ -373,11 +373,32 @@ def gemv_w8a16(x, b, b_scales, fmt=SCALE_F32_128x128, out=None, stream=None, fla
     return out
 
 
+def linear_fused_preferred(M: int, N: int, K: int, flags: int = 0) -> bool:
+    """Whether the one-launch quantising W8A8 kernel (fp8blk_linear_w8a8) beats
+    fp8blk_quant_act + fp8blk_gemm_w8a8 at this shape, from the measured
+    CUDA-graph rows of both forms at M = 2..32 on (N, K) = (4096, 4096),
+    (7168, 2048), (2048, 7168), (256, 512), with and without programmatic
+    dependent launch: one launch wins for small layers (N*K <= 2^21) at every
+    M <= 32, for M <= 2, for M <= 4 unless K > 4096 without PDL, and for
+    M <= 8 when K <= 4096 (K <= 2048 with PDL); elsewhere the quantiser's
+    per-row work inside every weight tile's pipeline costs more than the
+    saved launch and round trip."""
+    if M < 1 or M > LINEAR_FUSED_MAX_M:
+        return False
+    pdl = bool(int(flags) & FLAG_PDL)
+    if N * K <= 1 << 21 or M <= 2:
+        return True
+    if M <= 4:
+        return pdl or K <= 4096
+    return M <= 8 and K <= (2048 if pdl else 4096)
+
+
 def linear_w8a8(x, b, b_scales, out=None, stream=None, flags=0, out_dtype=None):
-    """bf16 x -> per-token quantisation -> W8A8 GEMM: one fused launch for
-    M <= 32, else quant_act + gemm_w8a8 (two launches)."""
+    """bf16 x -> per-token quantisation -> W8A8 GEMM: the fused one-launch
+    kernel where linear_fused_preferred says it is faster, else quant_act +
+    gemm_w8a8 (two launches, an e4m3 copy of x in between)."""
     import torch
-    if x.shape[0] <= LINEAR_FUSED_MAX_M:
+    if linear_fused_preferred(x.shape[0], b.shape[0], x.shape[1], flags):
         if out is None:
             out = torch.empty((x.shape[0], b.shape[0]), dtype=out_dtype or torch.bfloat16, device=x.device)
         fp8blk_linear_w8a8(x, b, b_scales, out, stream, flags)

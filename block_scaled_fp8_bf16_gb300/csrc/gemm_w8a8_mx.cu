@@ -97,6 +97,7 @@ constexpr int kStageA = BM * BK;
 constexpr int kStageB = BN * BK;
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kSfSlots = 4;           // K blocks of scale factors in TMEM ahead of the MMA
+constexpr int kSfAhead = 4;           // K blocks of scale factors in registers ahead of the TMEM writes
 constexpr int kSfCols = 4 + BN / 32;  // A: one column per lane quarter; B: one per 32 columns
 constexpr uint32_t kAccCols = BN;
 constexpr uint32_t kTmemCols = 512;
@@ -253,20 +254,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nb0 = n0 / 32;
     griddep_wait();                   // the activation exponents may be the previous kernel's output
     bool ok = true;
-    for (int kb = 0; kb < kblocks; ++kb) {
-      const int ss = kb % kSfSlots;
-      // Loads first: they do not touch the slot.
-      uint32_t wa = 0x7F7F7F7Fu;      // rows past M: scale 1 (their A rows are zero)
+    // The exponent words of K block kb are loaded kSfAhead blocks before they
+    // are written to TMEM, so the loads' latency overlaps the MMAs of the
+    // blocks in between (rows past M and columns past N: scale 1).
+    auto load_sf = [&](int kb, uint32_t& wa, uint32_t* wb) {
+      wa = 0x7F7F7F7Fu;
       if (m < M) {
         wa = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) wa |= uint32_t(__ldg(ea + int64_t(4 * kb + j) * lde + m)) << (8 * j);
       }
-      uint32_t wb[BN / 32];
 #pragma unroll
       for (int j = 0; j < BN / 32; ++j)
         wb[j] = (nb0 + j) * 32 < N ? __ldg(reinterpret_cast<const uint32_t*>(eb + int64_t(nb0 + j) * kw + 4 * kb))
                                    : 0x7F7F7F7Fu;
+    };
+    uint32_t qa[kSfAhead], qb[kSfAhead][BN / 32];
+#pragma unroll
+    for (int i = 0; i < kSfAhead; ++i)
+      if (i < kblocks) load_sf(i, qa[i], qb[i]);
+    for (int kb = 0; kb < kblocks; ++kb) {
+      const int ss = kb % kSfSlots;
+      const uint32_t wa = qa[0];
+      uint32_t wb[BN / 32];
+#pragma unroll
+      for (int j = 0; j < BN / 32; ++j) wb[j] = qb[0][j];
+#pragma unroll
+      for (int i = 0; i + 1 < kSfAhead; ++i) {
+        qa[i] = qa[i + 1];
+#pragma unroll
+        for (int j = 0; j < BN / 32; ++j) qb[i][j] = qb[i + 1][j];
+      }
+      if (kb + kSfAhead < kblocks) load_sf(kb + kSfAhead, qa[kSfAhead - 1], qb[kSfAhead - 1]);
       if (!__all_sync(0xffffffffu, mbar_wait(&sf_empty[ss], ((kb / kSfSlots) & 1) ^ 1, abort_flag))) {
         raise_error(err, abort_flag, kSiteDecodeAEmpty);
         ok = false;

@@ -238,3 +238,17 @@ def test_ue8m0_w8a8_argument_errors(fp8blk):
     assert g(eb=ctypes.c_void_p(16 * 1024 + 4)) == 3
     assert g(ldc=260) == 3              # bf16 rows need ldc * 2 % 16 == 0
     assert g(ldc=260, flags=2) != 3     # float32 rows of that pitch are fine
+
+
+def test_linear_fused_rule(fp8blk):
+    """The binding's choice between the one-launch quantising W8A8 kernel and
+    quant + GEMM (taken from measured rows of both forms)."""
+    pdl = fp8blk.FLAG_PDL
+    pref = fp8blk.linear_fused_preferred
+    assert pref(16, 256, 512) and pref(32, 256, 512)            # small layers: one launch at every M <= 32
+    assert pref(1, 4096, 4096) and pref(2, 2048, 7168)
+    assert pref(4, 2048, 7168, pdl) and not pref(4, 2048, 7168)
+    assert pref(8, 4096, 4096) and not pref(8, 4096, 4096, pdl)
+    assert pref(8, 7168, 2048, pdl) and not pref(8, 2048, 7168)
+    assert not pref(16, 4096, 4096) and not pref(32, 7168, 2048, pdl)
+    assert not pref(33, 256, 512) and not pref(0, 256, 512)
