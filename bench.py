@@ -590,12 +590,13 @@ def sweep(out_path, kinds=None):
         R = _rot_copies(per, l2, cap=32)
         x = tg.activations(1, M, K)
         b, eb = tg.ue8m0_weights(1, N, K)
+        bsf = fp8blk.ue8m0_weight_sf(eb)     # offline: the weight exponents in the tiled scale layout
         sets = []
         for _ in range(R):
             a, e = fp8blk.quant_act_ue8m0(x)
-            sets.append({"x": x.clone(), "a": a, "e": e, "b": b.clone(), "eb": eb.clone(),
+            sets.append({"x": x.clone(), "a": a, "e": e, "b": b.clone(), "eb": bsf.clone(),
                          "c": torch.empty((M, N), dtype=torch.bfloat16, device="cuda")})
-        byt = M * K + (K // 32) * M + N * K + (N // 32) * (K // 32) + 2 * M * N
+        byt = M * K + e.numel() + N * K + bsf.numel() + 2 * M * N
         calls = [lambda s=s: fp8blk.fp8blk_gemm_w8a8_ue8m0(s["a"], s["e"], s["b"], s["eb"], s["c"]) for s in sets]
         record("w8a8_ue8m0_gemm", M, N, K, graph_time(calls), 2.0 * M * N * K, byt, fp8_peak)
         calls = [lambda s=s: (fp8blk.fp8blk_quant_act_ue8m0(s["x"], s["a"], s["e"]),
@@ -653,11 +654,12 @@ def run_case(spec: str, iters: int):
         M, N, K = v
         x = tg.activations(1, M, K)
         b, eb = tg.ue8m0_weights(1, N, K)
+        bsf = fp8blk.ue8m0_weight_sf(eb)
         a, e = fp8blk.quant_act_ue8m0(x)
         c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         for _ in range(iters):
             fp8blk.fp8blk_quant_act_ue8m0(x, a, e)
-            fp8blk.fp8blk_gemm_w8a8_ue8m0(a, e, b, eb, c)
+            fp8blk.fp8blk_gemm_w8a8_ue8m0(a, e, b, bsf, c)
     elif kind == "w8a16":
         M, N, K, fmt = v
         x = tg.activations(1, M, K)

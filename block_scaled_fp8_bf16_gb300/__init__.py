@@ -51,8 +51,10 @@ EXPORTS = {
     "fp8blk_linear_w8a8": (_I32, [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_gemm_w8a8_grouped": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _I64, _U32,
                                          _P]),
-    "fp8blk_quant_act_ue8m0": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
-    "fp8blk_gemm_w8a8_ue8m0": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _U32, _P]),
+    "fp8blk_ue8m0_sf_bytes": (_I64, [_I64, _I64]),
+    "fp8blk_quant_act_ue8m0": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "fp8blk_ue8m0_weight_sf": (_I32, [_P, _I64, _I64, _P, _P]),
+    "fp8blk_gemm_w8a8_ue8m0": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_gemm_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_gemv_w8a16": (_I32, [_P, _I64, _P, _I64, _P, _I32, _P, _I64, _I64, _I64, _I64, _U32, _P]),
     "fp8blk_quant_weight": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P]),
@@ -161,31 +163,56 @@ def fp8blk_quant_act(x, a, a_scales, stream=None):
                                 _stream(stream)), "fp8blk_quant_act")
 
 
-def fp8blk_quant_act_ue8m0(x, a, a_exps, stream=None):
-    """x [M, K] bf16 -> a [M, K] e4m3 (uint8 view), a_exps [K/32, lde] uint8
-    (one power-of-two exponent byte per token per 32 values)."""
+def fp8blk_ue8m0_sf_bytes(rows, K):
+    """Bytes of a UE8M0 scale array in the tiled layout (rows padded to 128)."""
+    n = _L().fp8blk_ue8m0_sf_bytes(rows, K)
+    if n < 0:
+        raise ValueError(f"fp8blk_ue8m0_sf_bytes: no tiled scale layout for rows={rows}, K={K}")
+    return n
+
+
+def _sf_buffer(t, rows, K, name):
+    import torch
+    _expect(t, (torch.uint8,), name)
+    if not t.is_contiguous() or t.numel() < fp8blk_ue8m0_sf_bytes(rows, K):
+        raise ValueError(f"{name}: a contiguous uint8 buffer of fp8blk_ue8m0_sf_bytes({rows}, {K}) bytes")
+
+
+def fp8blk_quant_act_ue8m0(x, a, a_sf, stream=None):
+    """x [M, K] bf16 -> a [M, K] e4m3 (uint8 view), a_sf: one power-of-two
+    exponent byte per token per 32 values, tiled scale layout."""
     import torch
     _expect(x, (torch.bfloat16,), "x")
-    _expect(a_exps, (torch.uint8,), "a_exps")
     a = _bytes_tensor(a)
     M, K = x.shape
-    _check(_L().fp8blk_quant_act_ue8m0(_ptr(x), M, K, _ld(x), _ptr(a), _ld(a), _ptr(a_exps), _ld(a_exps),
-                                      _stream(stream)), "fp8blk_quant_act_ue8m0")
+    _sf_buffer(a_sf, M, K, "a_sf")
+    _check(_L().fp8blk_quant_act_ue8m0(_ptr(x), M, K, _ld(x), _ptr(a), _ld(a), _ptr(a_sf), _stream(stream)),
+           "fp8blk_quant_act_ue8m0")
 
 
-def fp8blk_gemm_w8a8_ue8m0(a, a_exps, b, b_exps, c, stream=None, flags=0):
-    """C[M, N] (bf16, or float32 when c is float32) = a[M, K] e4m3 x b[N, K] e4m3
-    with 1x32 activation and 32x32 weight UE8M0 exponents, on the tensor
-    cores' block scaling."""
+def fp8blk_ue8m0_weight_sf(b_exps, b_sf, stream=None):
+    """b_exps [N/32, K/32] uint8 (32x32 block exponents) -> b_sf, per-column
+    exponents in the tiled scale layout."""
     import torch
-    _expect(a_exps, (torch.uint8,), "a_exps")
     _expect(b_exps, (torch.uint8,), "b_exps")
+    if not b_exps.is_contiguous():
+        raise ValueError("b_exps: packed [N/32, K/32]")
+    N, K = b_exps.shape[0] * 32, b_exps.shape[1] * 32
+    _sf_buffer(b_sf, N, K, "b_sf")
+    _check(_L().fp8blk_ue8m0_weight_sf(_ptr(b_exps), N, K, _ptr(b_sf), _stream(stream)), "fp8blk_ue8m0_weight_sf")
+
+
+def fp8blk_gemm_w8a8_ue8m0(a, a_sf, b, b_sf, c, stream=None, flags=0):
+    """C[M, N] (bf16, or float32 when c is float32) = a[M, K] e4m3 x b[N, K] e4m3
+    with 1x32 activation and 32x32 weight UE8M0 exponents (both in the tiled
+    scale layout), on the tensor cores' block scaling."""
     a, b = _bytes_tensor(a), _bytes_tensor(b)
     M, K = a.shape
     N = b.shape[0]
-    _check(_L().fp8blk_gemm_w8a8_ue8m0(_ptr(a), _ld(a), _ptr(a_exps), _ld(a_exps), _ptr(b), _ld(b), _ptr(b_exps),
-                                      _ptr(c), _ld(c), M, N, K, _out_flags(c, flags), _stream(stream)),
-           "fp8blk_gemm_w8a8_ue8m0")
+    _sf_buffer(a_sf, M, K, "a_sf")
+    _sf_buffer(b_sf, N, K, "b_sf")
+    _check(_L().fp8blk_gemm_w8a8_ue8m0(_ptr(a), _ld(a), _ptr(a_sf), _ptr(b), _ld(b), _ptr(b_sf), _ptr(c), _ld(c),
+                                      M, N, K, _out_flags(c, flags), _stream(stream)), "fp8blk_gemm_w8a8_ue8m0")
 
 
 def fp8blk_gemm_w8a8(a, a_scales, b, b_scales, c, stream=None, flags=0):
@@ -309,26 +336,47 @@ def quant_act(x, stream=None):
     return a, s
 
 
-def act_exps_pitch(M: int) -> int:
-    """Row pitch (bytes) of the [K/32, lde] activation exponent array: M
-    rounded up to 16."""
-    return (M + 15) // 16 * 16
+def ue8m0_sf_from_rows(e_rows, pad=127):
+    """[rows, K/32] exponent bytes -> the flat tiled scale layout (rows padded
+    to 128 with `pad`).  Pure indexing; any device."""
+    import torch
+    rows, G = e_rows.shape
+    R = (rows + 127) // 128
+    full = torch.full((R * 128, G), pad, dtype=torch.uint8, device=e_rows.device)
+    full[:rows] = e_rows
+    # row = 128 mb + 32 q + r, slice g = 4 kb + j  ->  [mb][kb][r][q][j]
+    return full.view(R, 4, 32, G // 4, 4).permute(0, 3, 2, 1, 4).contiguous().view(-1)
+
+
+def ue8m0_sf_to_rows(sf, rows, K):
+    """The tiled scale layout -> [rows, K/32] exponent bytes (a copy)."""
+    R, KB = (rows + 127) // 128, K // 128
+    t = sf[:R * KB * 512].view(R, KB, 32, 4, 4).permute(0, 3, 2, 1, 4)   # [mb][q][r][kb][j]
+    return t.reshape(R * 128, KB * 4)[:rows].contiguous()
 
 
 def quant_act_ue8m0(x, stream=None):
     import torch
     M, K = x.shape
     a = torch.empty((M, K), dtype=torch.uint8, device=x.device)
-    e = torch.empty((K // 32, act_exps_pitch(M)), dtype=torch.uint8, device=x.device)
-    fp8blk_quant_act_ue8m0(x, a, e, stream)
-    return a, e
+    sf = torch.empty(fp8blk_ue8m0_sf_bytes(M, K), dtype=torch.uint8, device=x.device)
+    fp8blk_quant_act_ue8m0(x, a, sf, stream)
+    return a, sf
 
 
-def gemm_w8a8_ue8m0(a, a_exps, b, b_exps, out=None, stream=None, flags=0, out_dtype=None):
+def ue8m0_weight_sf(b_exps, stream=None):
+    import torch
+    N, K = b_exps.shape[0] * 32, b_exps.shape[1] * 32
+    sf = torch.empty(fp8blk_ue8m0_sf_bytes(N, K), dtype=torch.uint8, device=b_exps.device)
+    fp8blk_ue8m0_weight_sf(b_exps, sf, stream)
+    return sf
+
+
+def gemm_w8a8_ue8m0(a, a_sf, b, b_sf, out=None, stream=None, flags=0, out_dtype=None):
     import torch
     if out is None:
         out = torch.empty((a.shape[0], b.shape[0]), dtype=out_dtype or torch.bfloat16, device=a.device)
-    fp8blk_gemm_w8a8_ue8m0(a, a_exps, b, b_exps, out, stream, flags)
+    fp8blk_gemm_w8a8_ue8m0(a, a_sf, b, b_sf, out, stream, flags)
     return out
 
 

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 
@@ -381,38 +382,57 @@ fp8blk_status fp8blk_linear_w8a8(const void* x_bf16, int64_t ldx, const void* b_
   return cuda_status(launch_gemm_w8a8(p, dev, s));
 }
 
+int64_t fp8blk_ue8m0_sf_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0 || K % 128 != 0) return -1;
+  const int64_t blocks = (rows + 127) / 128;
+  if (K > 0 && blocks > INT64_MAX / 512 / (K / 128)) return -1;
+  return blocks * (K / 128) * 512;
+}
+
 fp8blk_status fp8blk_quant_act_ue8m0(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* a_e4m3,
-                                     int64_t lda, uint8_t* a_exps, int64_t lde, fp8blk_stream_t stream) {
+                                     int64_t lda, uint8_t* a_sf, fp8blk_stream_t stream) {
   if (M < 0 || K < 0) return FP8BLK_ERR_INVALID_ARG;
   if (K % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
   if (M == 0 || K == 0) return FP8BLK_OK;
-  if (!x_bf16 || !a_e4m3 || !a_exps) return FP8BLK_ERR_INVALID_ARG;
-  if (ldx < K || lda < K || lde < M) return FP8BLK_ERR_INVALID_ARG;
-  if (!aligned16(x_bf16) || !aligned16(a_e4m3) || !aligned16(a_exps)) return FP8BLK_ERR_MISALIGNED;
-  if ((ldx * 2) % 16 != 0 || lda % 16 != 0 || lde % 16 != 0) return FP8BLK_ERR_MISALIGNED;
+  if (!x_bf16 || !a_e4m3 || !a_sf) return FP8BLK_ERR_INVALID_ARG;
+  if (ldx < K || lda < K) return FP8BLK_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(a_e4m3) || !aligned16(a_sf)) return FP8BLK_ERR_MISALIGNED;
+  if ((ldx * 2) % 16 != 0 || lda % 16 != 0) return FP8BLK_ERR_MISALIGNED;
   DeviceInfo dev;
   fp8blk_status st = device_info(dev);
   if (st != FP8BLK_OK) return st;
-  QuantActUe8m0Args p{x_bf16, ldx, M, K, a_e4m3, lda, a_exps, lde};
+  QuantActUe8m0Args p{x_bf16, ldx, M, K, a_e4m3, lda, a_sf};
   return cuda_status(launch_quant_act_ue8m0(p, dev, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-fp8blk_status fp8blk_gemm_w8a8_ue8m0(const void* a_e4m3, int64_t lda, const uint8_t* a_exps, int64_t lde,
-                                     const void* b_e4m3, int64_t ldb, const uint8_t* b_exps, void* c, int64_t ldc,
-                                     int64_t M, int64_t N, int64_t K, uint32_t flags, fp8blk_stream_t stream) {
+fp8blk_status fp8blk_ue8m0_weight_sf(const uint8_t* b_exps, int64_t N, int64_t K, uint8_t* b_sf,
+                                     fp8blk_stream_t stream) {
+  if (N < 0 || K < 0) return FP8BLK_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
+  if (N == 0 || K == 0) return FP8BLK_OK;
+  if (!b_exps || !b_sf) return FP8BLK_ERR_INVALID_ARG;
+  if (!aligned16(b_exps) || !aligned16(b_sf)) return FP8BLK_ERR_MISALIGNED;
+  DeviceInfo dev;
+  fp8blk_status st = device_info(dev);
+  if (st != FP8BLK_OK) return st;
+  return cuda_status(launch_ue8m0_weight_sf(b_exps, N, K, b_sf, dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fp8blk_status fp8blk_gemm_w8a8_ue8m0(const void* a_e4m3, int64_t lda, const uint8_t* a_sf, const void* b_e4m3,
+                                     int64_t ldb, const uint8_t* b_sf, void* c, int64_t ldc, int64_t M, int64_t N,
+                                     int64_t K, uint32_t flags, fp8blk_stream_t stream) {
   if (M < 0 || N < 0 || K < 0 || (flags & ~kKnownFlags) != 0) return FP8BLK_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
   if (M > kIntMax || N > kIntMax || K > kIntMax) return FP8BLK_ERR_UNSUPPORTED_SHAPE;
   if (M == 0 || N == 0) return FP8BLK_OK;
   if (!c) return FP8BLK_ERR_INVALID_ARG;
-  if (K > 0 && (!a_e4m3 || !a_exps || !b_e4m3 || !b_exps)) return FP8BLK_ERR_INVALID_ARG;
-  if (lda < K || ldb < K || ldc < N || lde < M) return FP8BLK_ERR_INVALID_ARG;
-  if ((a_e4m3 && !aligned16(a_e4m3)) || (a_exps && !aligned16(a_exps)) || (b_e4m3 && !aligned16(b_e4m3)) ||
-      (b_exps && !aligned16(b_exps)) || !aligned16(c))
+  if (K > 0 && (!a_e4m3 || !a_sf || !b_e4m3 || !b_sf)) return FP8BLK_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldc < N) return FP8BLK_ERR_INVALID_ARG;
+  if ((a_e4m3 && !aligned16(a_e4m3)) || (a_sf && !aligned16(a_sf)) || (b_e4m3 && !aligned16(b_e4m3)) ||
+      (b_sf && !aligned16(b_sf)) || !aligned16(c))
     return FP8BLK_ERR_MISALIGNED;
   const bool f32 = (flags & FP8BLK_FLAG_OUT_F32) != 0;
-  if (lda % 16 != 0 || ldb % 16 != 0 || (ldc * (f32 ? 4 : 2)) % 16 != 0 || lde % 16 != 0)
-    return FP8BLK_ERR_MISALIGNED;
+  if (lda % 16 != 0 || ldb % 16 != 0 || (ldc * (f32 ? 4 : 2)) % 16 != 0) return FP8BLK_ERR_MISALIGNED;
   DeviceInfo dev;
   fp8blk_status st = device_info(dev);
   if (st != FP8BLK_OK) return st;
@@ -428,9 +448,8 @@ fp8blk_status fp8blk_gemm_w8a8_ue8m0(const void* a_e4m3, int64_t lda, const uint
   else
     st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c, uint64_t(N), uint64_t(M), uint64_t(ldc) * 2, 64, 32);
   if (st != FP8BLK_OK) return st;
-  p.ea = a_exps;
-  p.lde = lde;
-  p.eb = b_exps;
+  p.a_sf = a_sf;
+  p.b_sf = b_sf;
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);

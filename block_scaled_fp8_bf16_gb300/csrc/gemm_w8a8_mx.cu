@@ -1,6 +1,6 @@
 // W8A8 in the 32x32 UE8M0 format on hardware block scaling, sm_103a.
 //
-//   C[m, n] = sum_k A[m, k] 2^(ea[k/32, m] - 127) * B[n, k] 2^(eb[n/32, k/32] - 127)
+//   C[m, n] = sum_k A[m, k] 2^(ea[m, k/32] - 127) * B[n, k] 2^(eb[n/32, k/32] - 127)
 //
 // The weight format is one power-of-two scale per 32x32 block ("SM70 FP8
 // block-32 kernels (PLI Labs)", "How it works"); the activations get one
@@ -12,33 +12,44 @@
 // block_scale scale_vec::1X applies the two scales to each K = 32 slice and
 // accumulates the whole K range in TMEM.
 //
-// quant_act_ue8m0_kernel: bf16 x -> e4m3 codes + exponent bytes, one thread
-// per 32-value group: e is the smallest integer with 448 * 2^e >= amax
+// Scale operands are kept in the tiled layout the MMA consumes (one byte per
+// row -- token or weight column -- per 32 values of K): for 128 rows and one
+// 128-wide K block, 512 bytes [r][q][j] with row = 32 q + r and slice j of the
+// block, so byte (row, g) sits at
+//   ((row / 128) * (K / 128) + g / 4) * 512 + (row % 32) * 16 + ((row / 32) % 4) * 4 + g % 4.
+// One such 512-byte block, copied into TMEM by tcgen05.cp 32x128b.warpx4
+// (row r into lanes r, 32 + r, 64 + r, 96 + r, four columns), puts row
+// 32 q + r's four slice bytes at lane 32 q + r, column q: where the MMA reads
+// an A row's scale (lane m, column m / 32) and, for the B side, column n's
+// scale (lane 32 (m / 32) + n % 32, column n / 32; layout measured with
+// one-hot operands and distinct exponents per lane, column and byte).  The
+// 32x32 weight exponents become this layout once per weight, each block's
+// byte repeated for its 32 columns.
+//
+// quant_act_ue8m0_kernel: bf16 x -> e4m3 codes + tiled exponent bytes, one
+// thread per 32-value group: e is the smallest integer with 448 * 2^e >= amax
 // (from amax's exponent and whether its mantissa exceeds 1.75 = 448 / 2^8),
 // clamped to [-127, 126] (bf16 inputs never pass 120), and q =
-// e4m3(x * 2^-e), exact before the rounding, never saturating.
+// e4m3(x * 2^-e), exact before the rounding, never saturating.  Rows past M
+// in the last 128-row block get the byte 127 (scale 1).
 //
-// w8a8_mx_kernel: one 128 x 256 output tile per CTA.
-//   warp 0      TMA producer: A [128 rows x 128 B] and B [256 rows x 128 B]
-//               per 128-K block into a 4-stage ring.
-//   warp 1      TMEM allocation (512 columns); one thread issues the four
-//               K = 32 MMAs of each block (scale-factor byte j of the
-//               block's scale words for slice j) into the 256-column
-//               accumulator.
-//   warps 4..7  scale-factor writers, then the epilogue.  Warp q (lane
-//               quarter q) writes, per K block, into a ring of TMEM scale
-//               slots: its 32 rows' activation exponent words (four bytes:
-//               the block's four slices) at lane m, column q of the A slot,
-//               and the tile's eight 32-row weight exponent words at its
-//               lanes, columns 0..7 of the B slot.  The MMA reads row m's A
-//               scale at (lane m, column m / 32) and column n's B scale at
-//               (lane 32 (m / 32) + n % 32, column n / 32): every lane
-//               quarter holds the B scales of all 256 columns (layout
-//               measured with one-hot operands and distinct exponents per
-//               lane, column and byte).  At the end each warp reads its 32
-//               accumulator rows, rounds to bf16 (or keeps float32) and
-//               stores them with TMA tensor stores from a swizzled staging
-//               box.
+// ue8m0_weight_sf_kernel: [N/32][K/32] weight exponent bytes -> the tiled
+// per-column layout.
+//
+// w8a8_mx_kernel: persistent, one CTA per SM over 128 x 256 output tiles.
+//   warp 0      TMA producer: per 128-K block A [128 rows x 128 B], B
+//               [256 rows x 128 B] and the three 512-byte scale blocks (A;
+//               B columns 0..127 and 128..255) into a 4-stage ring, one
+//               barrier per stage.
+//   warp 1      TMEM allocation (512 columns: the 256-column accumulator and
+//               four scale slots of 12 columns); one thread copies the
+//               stage's scale blocks into its TMEM slot with tcgen05.cp and
+//               issues the four K = 32 MMAs of the block (scale byte j for
+//               slice j); the copies and the MMAs of one thread run in order.
+//   warps 4..7  epilogue: the accumulator rows of their lane quarter into
+//               registers (bf16), the accumulator released for the next tile,
+//               then TMA tensor stores from a swizzled staging box while the
+//               next tile's MMAs run.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -58,15 +69,25 @@ __device__ __forceinline__ int act_exponent(float amax) {
   return e < -127 ? -127 : (e > 126 ? 126 : e);
 }
 
+// Byte offset of (row, slice g) in the tiled scale layout (kb_count = K / 128).
+__host__ __device__ __forceinline__ int64_t sf_offset(int64_t row, int64_t g, int64_t kb_count) {
+  return ((row >> 7) * kb_count + (g >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (g & 3);
+}
+
 __global__ void __launch_bounds__(256) quant_act_ue8m0_kernel(const __nv_bfloat16* __restrict__ x, int64_t M,
                                                               int64_t K, int64_t ldx, uint8_t* __restrict__ a,
-                                                              int64_t lda, uint8_t* __restrict__ ex, int64_t lde) {
+                                                              int64_t lda, uint8_t* __restrict__ sf) {
   griddep_launch_dependents();
   const int64_t groups = K / 32;
-  const int64_t total = M * groups;
+  const int64_t kb_count = K / 128;
+  const int64_t total = (M + 127) / 128 * 128 * groups;   // rows padded to the 128-row block
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int64_t m = i / groups, g = i % groups;
+    if (m >= M) {
+      sf[sf_offset(m, g, kb_count)] = 127;
+      continue;
+    }
     const uint4* src = reinterpret_cast<const uint4*>(x + m * ldx + g * 32);
     float f[32];
 #pragma unroll
@@ -83,7 +104,24 @@ __global__ void __launch_bounds__(256) quant_act_ue8m0_kernel(const __nv_bfloat1
     uint4* dst = reinterpret_cast<uint4*>(a + m * lda + g * 32);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    ex[g * lde + m] = uint8_t(e + 127);
+    sf[sf_offset(m, g, kb_count)] = uint8_t(e + 127);
+  }
+}
+
+// One thread per 4-byte word of the tiled layout: the word of (128-column
+// block nb, K block kb, row r, column group c) holds the four slice bytes of
+// 32-column block 4 nb + c, the same for every r.
+__global__ void __launch_bounds__(256) ue8m0_weight_sf_kernel(const uint8_t* __restrict__ eb, int64_t N, int64_t K,
+                                                              uint32_t* __restrict__ sf) {
+  const int64_t kb_count = K / 128;
+  const int64_t kw = K / 32;
+  const int64_t words = N / 128 * kb_count * 128;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t w = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; w < words; w += stride) {
+    const int64_t chunk = w >> 7;
+    const int64_t c = w & 3;
+    const int64_t nb = chunk / kb_count, kb = chunk % kb_count;
+    sf[w] = *reinterpret_cast<const uint32_t*>(eb + (nb * 4 + c) * kw + 4 * kb);
   }
 }
 
@@ -92,23 +130,25 @@ __global__ void __launch_bounds__(256) quant_act_ue8m0_kernel(const __nv_bfloat1
 constexpr int BM = 128;               // rows of A / C per tile
 constexpr int BN = 256;               // rows of B (columns of C) per tile
 constexpr int BK = 128;               // K per stage: four K = 32 MMAs, one scale word
-constexpr int kStages = 4;
+constexpr int kStages = 4;            // operand stages; also the ring of TMEM scale slots
 constexpr int kStageA = BM * BK;
 constexpr int kStageB = BN * BK;
 constexpr int kStageBytes = kStageA + kStageB;
-constexpr int kSfSlots = 4;           // K blocks of scale factors in TMEM ahead of the MMA
-constexpr int kSfAhead = 4;           // K blocks of scale factors in registers ahead of the TMEM writes
 constexpr int kSfCols = 4 + BN / 32;  // A: one column per lane quarter; B: one per 32 columns
 constexpr uint32_t kAccCols = BN;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kThreads = 256;         // warps 0..3 control, 4..7 scale writers + epilogue
+constexpr int kThreads = 256;         // warps 0..3 control, 4..7 epilogue
+constexpr int kSfBytes = 3 * 512;     // per stage: the A scale block, then B's for columns 0..127 and 128..255
 constexpr int kStageC = 32 * 128;     // a warp's 32-row x 128-byte output box
-constexpr size_t kCOff = size_t(kStages) * kStageBytes;
-constexpr size_t kBarOff = kCOff + 4 * size_t(kStageC);
+constexpr int kCBufs = 1;             // output boxes in flight per epilogue warp
+constexpr size_t kSfOff = size_t(kStages) * kStageBytes;
+constexpr size_t kCOff = kSfOff + size_t(kStages) * kSfBytes;
+constexpr size_t kBarOff = kCOff + size_t(4 * kCBufs) * kStageC;
 constexpr size_t kSmemBytes = kBarOff + 256 + 1024;
-static_assert(kAccCols + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
+static_assert(kAccCols + kStages * kSfCols <= kTmemCols, "TMEM budget");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "swizzle atoms");
+static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0 && kCOff % 1024 == 0, "swizzle atoms");
+static_assert(kSfOff % 128 == 0 && kSfBytes % 128 == 0, "scale blocks: 16-byte aligned copies");
 
 // kind::mxf8f6f4 instruction descriptor: B scale byte [4,6), e4m3 A and B
 // (format 0), both K-major, N >> 3 at [17,23), scale type UE8M0 (bit 23),
@@ -128,56 +168,90 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
 }
 
-__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+// Shared-memory descriptor of a 32-row x 16-byte block without swizzle: rows
+// of 16 bytes, 8-row core matrices 128 bytes apart (both offset fields 128 B;
+// there is one core matrix along the 16 bytes), descriptor version 1.
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
 }
 
-__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t* r) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
+// Copies 32 rows x 128 bits of shared memory into TMEM columns [taddr,
+// taddr + 4), the same rows into each of the four lane quarters (row r to
+// lanes r, 32 + r, 64 + r, 96 + r).  Issued by the MMA thread, so it is
+// ordered with the MMAs that read the columns.
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
+
+// Waits until at most kCBufs - 1 of the thread's committed bulk stores are
+// still reading shared memory (the oldest staging buffer is free).
+__device__ __forceinline__ void wait_staging() {
+  if constexpr (kCBufs == 1)
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  else
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+static_assert(kCBufs == 1 || kCBufs == 2, "staging buffers");
 
 __device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, int site) {
   *abort_flag = 1;
   atomicCAS(err, 0, kDevErrW8A8Mx | site);
 }
 
+// Tile t of the row-major tile grid (columns fastest).
+__device__ __forceinline__ void mx_tile(int t, int n_tiles, int& m0, int& n0) {
+  const int mt = t / n_tiles;
+  m0 = mt * BM;
+  n0 = (t - mt * n_tiles) * BN;
+}
+
+// One persistent CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// Per K block ("it" counts K blocks over all of the CTA's tiles; stage and
+// scale slot are it % kStages):
+//   warp 0 (producer)  waits empty[s], loads A, B and the three scale blocks
+//                      into stage s (one barrier, full[s], with all the bytes);
+//   warp 1 (issuer)    waits full[s], copies the scale blocks into TMEM slot s,
+//                      issues the four K = 32 MMAs and commits empty[s]; after
+//                      a tile's last block it commits acc_full, and before a
+//                      tile's first block it waits for acc_empty;
+//   warps 4..7         wait acc_full, read the 32 x 256 accumulator rows of
+//                      their lane quarter into registers, release the
+//                      accumulator (acc_empty) and only then store the tile,
+//                      so the next tile's MMAs overlap the stores.
+// A scale slot is rewritten only after empty[s] (the MMAs that read it have
+// completed) and the next full[s].
 template <bool F32>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const uint8_t* __restrict__ ea, int64_t lde,
-                   const uint8_t* __restrict__ eb, int M, int N, int K, int* __restrict__ err) {
+                   const __grid_constant__ CUtensorMap tmC, const uint8_t* __restrict__ a_sf,
+                   const uint8_t* __restrict__ b_sf, int M, int N, int K, int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* empty = full + kStages;
-  uint64_t* sf_full = empty + kStages;
-  uint64_t* sf_empty = sf_full + kSfSlots;
-  uint64_t* acc_full = sf_empty + kSfSlots;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_tiles = (N + BN - 1) / BN;
-  const int mt = blockIdx.x / n_tiles;
-  const int nt = blockIdx.x % n_tiles;
-  const int m0 = mt * BM, n0 = nt * BN;
+  const int num_tiles = ((M + BM - 1) / BM) * n_tiles;
   const int kblocks = K / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int s = 0; s < kSfSlots; ++s) {
-      mbar_init(&sf_full[s], 4);   // the four scale-writer warps
-      mbar_init(&sf_empty[s], 1);  // MMA commit
+      mbar_init(&full[s], 1);    // producer, with the bytes
+      mbar_init(&empty[s], 1);   // MMA commit
     }
     mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);     // the four epilogue warps
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -196,151 +270,170 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const uint32_t sf_base = tmem + kAccCols;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      griddep_wait();   // A may be the previous kernel's output
-      int kb = 0;
-      for (; kb < kblocks; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag)) {
-          raise_error(err, abort_flag, kSiteProducerEmpty);
-          break;
+  if (warp < 4) {
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
+      griddep_wait();   // A and its scales may be the previous kernel's output
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int m0, n0;
+        mx_tile(t, n_tiles, m0, n0);
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = int(it % kStages);
+          if (!mbar_wait(&empty[s], ((it / kStages) & 1u) ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteProducerEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + size_t(s) * kStageBytes;
+          uint8_t* sf = smem + kSfOff + size_t(s) * kSfBytes;
+          // B columns past N (a 128-column last tile): the first half's scales
+          // again, so that every slot holds finite scales (B is zero there).
+          const uint8_t* sfb0 = b_sf + (int64_t(n0 / 128) * kblocks + kb) * 512;
+          const uint8_t* sfb1 = n0 + 128 < N ? sfb0 + int64_t(kblocks) * 512 : sfb0;
+          mbar_arrive_expect_tx(&full[s], kStageBytes + kSfBytes);
+          tma_load_2d(sa, &tmA, &full[s], kb * BK, m0);
+          tma_load_2d(sa + kStageA, &tmB, &full[s], kb * BK, n0);
+          tma_load_2d(sa + kStageA + kStageB / 2, &tmB, &full[s], kb * BK, n0 + BN / 2);
+          bulk_copy_g2s(sf, a_sf + (int64_t(m0 / 128) * kblocks + kb) * 512, 512, &full[s]);
+          bulk_copy_g2s(sf + 512, sfb0, 512, &full[s]);
+          bulk_copy_g2s(sf + 1024, sfb1, 512, &full[s]);
         }
-        uint8_t* sa = smem + size_t(s) * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tma_load_2d(sa, &tmA, &full[s], kb * BK, m0);
-        tma_load_2d(sa + kStageA, &tmB, &full[s], kb * BK, n0);
-        tma_load_2d(sa + kStageA + kStageB / 2, &tmB, &full[s], kb * BK, n0 + BN / 2);
       }
-      if (kb < kblocks) {
-        const int first = kb > kStages ? kb - kStages : 0;
-        for (int j = first; j < kb; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1, nullptr);
+      if (!ok) {
+        // Copies still in flight complete on full[]: wait for their bytes
+        // (bounded) before the CTA can exit.
+        const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1u, nullptr);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int s = kb % kStages;
-        const int ss = kb % kSfSlots;
-        if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag)) {
-          raise_error(err, abort_flag, kSiteMmaFull);
-          break;
-        }
-        if (!mbar_wait(&sf_full[ss], (kb / kSfSlots) & 1, abort_flag)) {
-          raise_error(err, abort_flag, kSiteMmaAFull);
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      uint32_t it = 0;
+      bool ok = true;
+      int i = 0;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++i) {
+        if (!mbar_wait(acc_empty, (uint32_t(i) & 1u) ^ 1u, abort_flag)) {
+          raise_error(err, abort_flag, kSiteMmaAccEmpty);
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(smem + size_t(s) * kStageBytes);
-        const uint32_t b0 = a0 + kStageA;
-        const uint32_t sfa = sf_base + uint32_t(ss * kSfCols);
-        const uint32_t sfb = sfa + 4u;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = int(it % kStages);
+          if (!mbar_wait(&full[s], (it / kStages) & 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaFull);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + size_t(s) * kStageBytes);
+          const uint32_t b0 = a0 + kStageA;
+          const uint32_t sfa = sf_base + uint32_t(s * kSfCols);
+          const uint32_t sfb = sfa + 4u;
+          const uint32_t sfs = smem_u32(smem + kSfOff + size_t(s) * kSfBytes);
+          tmem_cp_sf(sfa, sf_desc(sfs));
+          tmem_cp_sf(sfb, sf_desc(sfs + 512u));
+          tmem_cp_sf(sfb + 4u, sf_desc(sfs + 1024u));
 #pragma unroll
-        for (int j = 0; j < BK / 32; ++j)
-          mma_mx(tmem, desc_sw128_kmajor(a0 + 32u * j), desc_sw128_kmajor(b0 + 32u * j), mx_idesc(BM, BN, uint32_t(j)),
-                 sfa, sfb, (kb > 0 || j > 0) ? 1u : 0u);
-        mma_commit(&empty[s]);
-        mma_commit(&sf_empty[ss]);
+          for (int j = 0; j < BK / 32; ++j)
+            mma_mx(tmem, desc_sw128_kmajor(a0 + 32u * j), desc_sw128_kmajor(b0 + 32u * j),
+                   mx_idesc(BM, BN, uint32_t(j)), sfa, sfb, (kb > 0 || j > 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(acc_full);
       }
-      mma_commit(acc_full);   // also after an abort: the epilogue and the release of TMEM wait for it
+      // TMEM is released only after every MMA issued above has completed.
+      mma_commit(drain);
+      if (!mbar_wait(drain, 0, nullptr)) raise_error(err, abort_flag, kSiteDrain);
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ scale writers
+  } else {
+    // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    const int m = m0 + 32 * q + lane;
-    const int kw = K / 32;            // exponent bytes per weight row block
-    const int nb0 = n0 / 32;
-    griddep_wait();                   // the activation exponents may be the previous kernel's output
-    bool ok = true;
-    // The exponent words of K block kb are loaded kSfAhead blocks before they
-    // are written to TMEM, so the loads' latency overlaps the MMAs of the
-    // blocks in between (rows past M and columns past N: scale 1).
-    auto load_sf = [&](int kb, uint32_t& wa, uint32_t* wb) {
-      wa = 0x7F7F7F7Fu;
-      if (m < M) {
-        wa = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) wa |= uint32_t(__ldg(ea + int64_t(4 * kb + j) * lde + m)) << (8 * j);
-      }
-#pragma unroll
-      for (int j = 0; j < BN / 32; ++j)
-        wb[j] = (nb0 + j) * 32 < N ? __ldg(reinterpret_cast<const uint32_t*>(eb + int64_t(nb0 + j) * kw + 4 * kb))
-                                   : 0x7F7F7F7Fu;
-    };
-    uint32_t qa[kSfAhead], qb[kSfAhead][BN / 32];
-#pragma unroll
-    for (int i = 0; i < kSfAhead; ++i)
-      if (i < kblocks) load_sf(i, qa[i], qb[i]);
-    for (int kb = 0; kb < kblocks; ++kb) {
-      const int ss = kb % kSfSlots;
-      const uint32_t wa = qa[0];
-      uint32_t wb[BN / 32];
-#pragma unroll
-      for (int j = 0; j < BN / 32; ++j) wb[j] = qb[0][j];
-#pragma unroll
-      for (int i = 0; i + 1 < kSfAhead; ++i) {
-        qa[i] = qa[i + 1];
-#pragma unroll
-        for (int j = 0; j < BN / 32; ++j) qb[i][j] = qb[i + 1][j];
-      }
-      if (kb + kSfAhead < kblocks) load_sf(kb + kSfAhead, qa[kSfAhead - 1], qb[kSfAhead - 1]);
-      if (!__all_sync(0xffffffffu, mbar_wait(&sf_empty[ss], ((kb / kSfSlots) & 1) ^ 1, abort_flag))) {
-        raise_error(err, abort_flag, kSiteDecodeAEmpty);
-        ok = false;
+    const uint32_t lane_base = uint32_t(32 * q) << 16;
+    uint8_t* stg = smem + kCOff + size_t(q) * kCBufs * kStageC;
+    int i = 0;
+    uint32_t boxes = 0;   // output boxes this warp has stored (picks the staging buffer)
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++i) {
+      int m0, n0;
+      mx_tile(t, n_tiles, m0, n0);
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_full, uint32_t(i) & 1u, abort_flag))) {
+        raise_error(err, abort_flag, kSiteEpilogueFull);
         break;
       }
       tc_fence_after();
-      const uint32_t lane_base = uint32_t(32 * q) << 16;
-      const uint32_t sfa = sf_base + uint32_t(ss * kSfCols);
-      tmem_st_x1(sfa + lane_base + uint32_t(q), wa);
-      tmem_st_x8(sfa + lane_base + 4u, wb);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sf_full[ss]);
-    }
-    // ------------------------------------------------------------ epilogue
-    if (!__all_sync(0xffffffffu, mbar_wait(acc_full, 0, ok ? abort_flag : nullptr))) {
-      raise_error(err, abort_flag, kSiteEpilogueFull);
-    } else if (ok && !*abort_flag && m0 + 32 * q < M) {
-      tc_fence_after();
-      uint8_t* stg = smem + kCOff + size_t(q) * kStageC;
-      constexpr int kBoxCols = F32 ? 32 : 64;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += kBoxCols) {
-        if (n0 + c >= N) break;
-        uint32_t v[64];
-        const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(c);
-        tmem_ld_x32(taddr, v);
-        if constexpr (!F32) tmem_ld_x32(taddr + 32u, v + 32);
-        tmem_ld_wait();
-        if (lane == 0) bulk_wait_group_read0();   // the previous box has left the staging buffer
-        __syncwarp();
-        uint8_t* dst = stg + lane * 128;
+      const bool rows = m0 + 32 * q < M;
+      if constexpr (!F32) {
+        // The whole 32 x 256 block: TMEM -> bf16 pairs in registers, then the
+        // accumulator is released and the stores follow.
+        uint32_t packed[BN / 2];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint4 o;
-          if constexpr (F32) {
-            o = make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
-          } else {
-            o.x = pack_bf16x2(__uint_as_float(v[8 * ch]), __uint_as_float(v[8 * ch + 1]));
-            o.y = pack_bf16x2(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3]));
-            o.z = pack_bf16x2(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5]));
-            o.w = pack_bf16x2(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7]));
-          }
-          *reinterpret_cast<uint4*>(dst + ((ch ^ (lane & 7)) << 4)) = o;
+        for (int c = 0; c < BN; c += 64) {
+          uint32_t v[64];
+          tmem_ld_x32(tmem + lane_base + uint32_t(c), v);
+          tmem_ld_x32(tmem + lane_base + uint32_t(c + 32), v + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            packed[c / 2 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
         }
-        fence_async_shared();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmC, stg, n0 + c, m0 + 32 * q);
-          bulk_commit_group();
+        if (lane == 0) mbar_arrive(acc_empty);
+#pragma unroll
+        for (int b = 0; b < BN / 64; ++b) {
+          if (rows && n0 + 64 * b < N) {
+            uint8_t* box = stg + size_t(boxes % kCBufs) * kStageC;
+            if (lane == 0) wait_staging();   // the box stored kCBufs boxes ago has left this buffer
+            __syncwarp();
+            uint8_t* dst = box + lane * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(dst + ((ch ^ (lane & 7)) << 4)) =
+                  make_uint4(packed[32 * b + 4 * ch], packed[32 * b + 4 * ch + 1], packed[32 * b + 4 * ch + 2],
+                             packed[32 * b + 4 * ch + 3]);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, box, n0 + 64 * b, m0 + 32 * q);
+              bulk_commit_group();
+            }
+            ++boxes;
+          }
+        }
+      } else {
+        // float32 output: 32-column boxes straight from TMEM; the accumulator
+        // is released after the last read.
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem + lane_base + uint32_t(c), v);
+          tmem_ld_wait();
+          if (c + 32 == BN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+          }
+          if (rows && n0 + c < N) {
+            uint8_t* box = stg + size_t(boxes % kCBufs) * kStageC;
+            if (lane == 0) wait_staging();
+            __syncwarp();
+            uint8_t* dst = box + lane * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(dst + ((ch ^ (lane & 7)) << 4)) =
+                  make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, box, n0 + c, m0 + 32 * q);
+              bulk_commit_group();
+            }
+            ++boxes;
+          }
         }
       }
-      if (lane == 0) bulk_wait_group0();
     }
+    if (lane == 0) bulk_wait_group0();
   }
 
   __syncwarp();
@@ -355,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_quant_act_ue8m0(const QuantActUe8m0Args& p, const DeviceInfo& dev, cudaStream_t s) {
-  const int64_t total = p.M * (p.K / 32);
+  const int64_t total = (p.M + 127) / 128 * 128 * (p.K / 32);
   const int64_t want = (total + 255) / 256;
   const int64_t cap = int64_t(dev.num_sms) * 8;
   const unsigned grid = unsigned(want < cap ? want : cap);
@@ -364,12 +457,22 @@ cudaError_t launch_quant_act_ue8m0(const QuantActUe8m0Args& p, const DeviceInfo&
   cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = s;
   return cudaLaunchKernelEx(&cfg, quant_act_ue8m0_kernel, static_cast<const __nv_bfloat16*>(p.x), p.M, p.K, p.ldx,
-                            static_cast<uint8_t*>(p.a), p.lda, p.ex, p.lde);
+                            static_cast<uint8_t*>(p.a), p.lda, p.sf);
+}
+
+cudaError_t launch_ue8m0_weight_sf(const uint8_t* eb, int64_t N, int64_t K, uint8_t* sf, const DeviceInfo& dev,
+                                   cudaStream_t s) {
+  const int64_t words = N / 128 * (K / 128) * 128;
+  const int64_t want = (words + 255) / 256;
+  const int64_t cap = int64_t(dev.num_sms) * 8;
+  const unsigned grid = unsigned(want < cap ? want : cap);
+  ue8m0_weight_sf_kernel<<<grid, 256, 0, s>>>(eb, N, K, reinterpret_cast<uint32_t*>(sf));
+  return cudaGetLastError();
 }
 
 namespace {
 template <bool F32>
-cudaError_t launch_mx(const GemmW8A8MxArgs& p, const DeviceInfo&, cudaStream_t stream) {
+cudaError_t launch_mx(const GemmW8A8MxArgs& p, const DeviceInfo& dev, cudaStream_t stream) {
   static bool attr_done[64] = {};
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
@@ -381,8 +484,9 @@ cudaError_t launch_mx(const GemmW8A8MxArgs& p, const DeviceInfo&, cudaStream_t s
   }
   const int64_t tiles = int64_t((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const int64_t grid = tiles < dev.num_sms ? tiles : dev.num_sms;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(tiles), 1, 1);
+  cfg.gridDim = dim3(unsigned(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -391,7 +495,7 @@ cudaError_t launch_mx(const GemmW8A8MxArgs& p, const DeviceInfo&, cudaStream_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, w8a8_mx_kernel<F32>, p.tmA, p.tmB, p.tmC, p.ea, p.lde, p.eb, p.M, p.N, p.K, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a8_mx_kernel<F32>, p.tmA, p.tmB, p.tmC, p.a_sf, p.b_sf, p.M, p.N, p.K, p.err);
 }
 }  // namespace
 

@@ -116,18 +116,19 @@ struct QuantActUe8m0Args {
   int64_t M, K;
   void* a;            // e4m3 [M, K] pitch lda
   int64_t lda;
-  uint8_t* ex;        // exponent bytes [K/32][lde]
-  int64_t lde;
+  uint8_t* sf;        // exponent bytes in the tiled scale layout, rows padded to 128
 };
 cudaError_t launch_quant_act_ue8m0(const QuantActUe8m0Args& p, const DeviceInfo& dev, cudaStream_t s);
+// [N/32][K/32] weight exponent bytes -> the tiled per-column scale layout.
+cudaError_t launch_ue8m0_weight_sf(const uint8_t* eb, int64_t N, int64_t K, uint8_t* sf, const DeviceInfo& dev,
+                                   cudaStream_t s);
 
 struct GemmW8A8MxArgs {
   CUtensorMap tmA;    // e4m3 [M, K], box {128 (K), 128 (M)}, 128B swizzle
   CUtensorMap tmB;    // e4m3 [N, K], box {128 (K), 128 (N)}, 128B swizzle
   CUtensorMap tmC;    // C [M, N], box {128 bytes of N, 32 (M)}, 128B swizzle
-  const uint8_t* ea;  // activation exponent bytes [K/32][lde]
-  int64_t lde;
-  const uint8_t* eb;  // weight exponent bytes [N/32][K/32]
+  const uint8_t* a_sf;  // activation exponent bytes, tiled scale layout (rows padded to 128)
+  const uint8_t* b_sf;  // weight exponent bytes per column, tiled scale layout
   int M, N, K;
   bool pdl;
   bool out_f32;

@@ -89,7 +89,7 @@ typedef struct {
   int32_t max_split_k;        /* largest split-K cluster the kernels use */
 } fp8blk_constraints;
 
-#define FP8BLK_ABI_VERSION 2
+#define FP8BLK_ABI_VERSION 3
 
 /*
  * Launch flags of the three GEMM entry points (bitwise OR; 0 = none).
@@ -230,6 +230,23 @@ FP8BLK_API fp8blk_status fp8blk_gemm_w8a8_grouped(const void* a_e4m3, int64_t ld
                                uint32_t flags, fp8blk_stream_t stream);
 
 /*
+ * UE8M0 scale operands of the W8A8 product are stored in the tiled layout
+ * the tensor cores' block scaling reads (one exponent byte, 127 + e, per row
+ * -- token or weight column -- per 32 values of K).  For each 128-row block
+ * and each 128-wide K block, 512 bytes [r][q][j] with row = 32 q + r and
+ * slice j of the K block; byte (row, g) of a rows x K array is at
+ *
+ *   ((row / 128) * (K / 128) + g / 4) * 512 + (row % 32) * 16
+ *     + ((row / 32) % 4) * 4 + g % 4.
+ *
+ * The pages fix the exponents, not this byte order; it is the one the
+ * product's scale copies take without rearranging.
+ * fp8blk_ue8m0_sf_bytes: size of such an array for `rows` rows (padded to
+ * 128) and K; -1 when rows < 0, K < 0, K % 128 != 0 or the size overflows.
+ */
+FP8BLK_API int64_t fp8blk_ue8m0_sf_bytes(int64_t rows, int64_t K);
+
+/*
  * Per-token activation quantisation for W8A8 in the 32x32 UE8M0 weight
  * format: one power-of-two scale per token per 32 values of K, so that each
  * 1x32 activation slice meets one 32x32 weight block ("SM70 FP8 block-32
@@ -241,13 +258,24 @@ FP8BLK_API fp8blk_status fp8blk_gemm_w8a8_grouped(const void* a_e4m3, int64_t ld
  *
  *  x_bf16   [M, K] bf16, row pitch ldx elements (ldx*2 % 16 == 0).
  *  a_e4m3   [M, K] e4m3 out, row pitch lda bytes (lda % 16 == 0).
- *  a_exps   [K/32][lde] uint8 out, byte = e + 127, M contiguous;
- *           lde >= M, lde % 16 == 0.
+ *  a_sf     fp8blk_ue8m0_sf_bytes(M, K) bytes out, the tiled scale layout;
+ *           rows M .. 128*ceil(M/128)-1 get 127 (scale 1).
  *  K % 128 == 0 (the product consumes 128-wide K blocks), M >= 0 (0: no-op).
  *  All pointers 16-byte aligned.  Asynchronous on stream.
  */
 FP8BLK_API fp8blk_status fp8blk_quant_act_ue8m0(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
-                               void* a_e4m3, int64_t lda, uint8_t* a_exps, int64_t lde,
+                               void* a_e4m3, int64_t lda, uint8_t* a_sf,
+                               fp8blk_stream_t stream);
+
+/*
+ * Offline weight preparation for fp8blk_gemm_w8a8_ue8m0: the 32x32 block
+ * exponents b_exps [N/32][K/32] (the UE8M0 weight format of
+ * fp8blk_gemm_w8a16, packed) written as per-column scales in the tiled
+ * layout (each block's byte for its 32 columns), fp8blk_ue8m0_sf_bytes(N, K)
+ * bytes into b_sf.  N % 128 == 0, K % 128 == 0; 16-byte aligned pointers.
+ * Asynchronous on stream.
+ */
+FP8BLK_API fp8blk_status fp8blk_ue8m0_weight_sf(const uint8_t* b_exps, int64_t N, int64_t K, uint8_t* b_sf,
                                fp8blk_stream_t stream);
 
 /*
@@ -258,12 +286,11 @@ FP8BLK_API fp8blk_status fp8blk_quant_act_ue8m0(const void* x_bf16, int64_t M, i
  * 2^(ea - 127) * 2^(eb - 127) inside the MMA and accumulated in FP32, with
  * no software promotion.
  *
- *   C[m, n] = sum_k A[m, k] 2^(ea[k/32][m] - 127) * B[n, k] 2^(eb[n/32][k/32] - 127)
+ *   C[m, n] = sum_k A[m, k] 2^(ea[m, k/32] - 127) * B[n, k] 2^(eb[n/32, k/32] - 127)
  *
- *  a_e4m3, lda, a_exps, lde   as written by fp8blk_quant_act_ue8m0.
+ *  a_e4m3, lda, a_sf   as written by fp8blk_quant_act_ue8m0.
  *  b_e4m3   [N, K] e4m3 weights, K contiguous, row pitch ldb bytes.
- *  b_exps   [N/32][K/32] uint8 weight exponent bytes (the UE8M0 format of
- *           fp8blk_gemm_w8a16), packed.
+ *  b_sf     the weight exponents as written by fp8blk_ue8m0_weight_sf.
  *  c        [M, N] bf16 out (round to nearest even), row pitch ldc
  *           elements; float32 with FP8BLK_FLAG_OUT_F32.
  *  N % 128 == 0, K % 128 == 0, M >= 0 (0: no-op), K == 0 zero-fills C.
@@ -271,9 +298,8 @@ FP8BLK_API fp8blk_status fp8blk_quant_act_ue8m0(const void* x_bf16, int64_t M, i
  *  Weight codes are assumed finite and exponent bytes below 255 (the UE8M0
  *  NaN); fp8blk_validate_weights checks the stricter [-14, 7] window.
  */
-FP8BLK_API fp8blk_status fp8blk_gemm_w8a8_ue8m0(const void* a_e4m3, int64_t lda,
-                               const uint8_t* a_exps, int64_t lde,
-                               const void* b_e4m3, int64_t ldb, const uint8_t* b_exps,
+FP8BLK_API fp8blk_status fp8blk_gemm_w8a8_ue8m0(const void* a_e4m3, int64_t lda, const uint8_t* a_sf,
+                               const void* b_e4m3, int64_t ldb, const uint8_t* b_sf,
                                void* c, int64_t ldc, int64_t M, int64_t N, int64_t K,
                                uint32_t flags, fp8blk_stream_t stream);
 

@@ -6,6 +6,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -68,7 +69,7 @@ def test_no_cuda_driver_link_dependency(fp8blk):
 
 def test_constraints(fp8blk):
     c = fp8blk.fp8blk_query_constraints()
-    assert c["abi_version"] == 2
+    assert c["abi_version"] == 3
     assert c["scale_block_k"] == 128 and c["scale_block_n"] == 128 and c["ue8m0_block"] == 32
     assert c["gemv_max_m"] == 16 and c["ptr_align_bytes"] == 16 and c["lds_multiple"] == 4
 
@@ -214,30 +215,70 @@ def test_ue8m0_w8a8_argument_errors(fp8blk):
     L = fp8blk._L()
     P = ctypes.c_void_p(16 * 1024)
 
-    def q(M=16, K=512, ldx=512, lda=512, lde=16, x=P, e=P):
-        return L.fp8blk_quant_act_ue8m0(x, M, K, ldx, P, lda, e, lde, None)
+    def q(M=16, K=512, ldx=512, lda=512, x=P, e=P):
+        return L.fp8blk_quant_act_ue8m0(x, M, K, ldx, P, lda, e, None)
 
     assert q(M=-1) == 1
     assert q(K=96) == 2                 # K % 128
     assert q(M=0) == 0                  # no-op
     assert q(e=None) == 1
-    assert q(lde=8) == 1                # lde < M
-    assert q(lde=24) == 3               # exponent rows must be 16-byte multiples
+    assert q(lda=256) == 1              # lda < K
+    assert q(e=ctypes.c_void_p(16 * 1024 + 8)) == 3
     assert q(x=ctypes.c_void_p(16 * 1024 + 8)) == 3
     assert q(ldx=516) == 3
 
-    def g(M=16, N=256, K=512, lda=512, lde=16, ldb=512, ldc=256, flags=0, ea=P, eb=P, c=P):
-        return L.fp8blk_gemm_w8a8_ue8m0(P, lda, ea, lde, P, ldb, eb, c, ldc, M, N, K, flags, None)
+    def w(N=256, K=512, eb=P, sf=P):
+        return L.fp8blk_ue8m0_weight_sf(eb, N, K, sf, None)
+
+    assert w(N=96) == 2 and w(K=96) == 2
+    assert w(N=-128) == 1
+    assert w(N=0) == 0 and w(K=0) == 0  # no-ops
+    assert w(eb=None) == 1 and w(sf=None) == 1
+    assert w(sf=ctypes.c_void_p(16 * 1024 + 4)) == 3
+
+    def g(M=16, N=256, K=512, lda=512, ldb=512, ldc=256, flags=0, ea=P, eb=P, c=P):
+        return L.fp8blk_gemm_w8a8_ue8m0(P, lda, ea, P, ldb, eb, c, ldc, M, N, K, flags, None)
 
     assert g(N=96) == 2 and g(K=96) == 2
     assert g(M=-1) == 1 and g(flags=4) == 1
     assert g(M=0) == 0 and g(N=0) == 0  # no-ops, no device needed
     assert g(ea=None) == 1 and g(eb=None) == 1 and g(c=None) == 1
-    assert g(lde=8) == 1                # lde < M
-    assert g(lde=24) == 3
+    assert g(ldb=256) == 1              # ldb < K
     assert g(eb=ctypes.c_void_p(16 * 1024 + 4)) == 3
     assert g(ldc=260) == 3              # bf16 rows need ldc * 2 % 16 == 0
     assert g(ldc=260, flags=2) != 3     # float32 rows of that pitch are fine
+
+
+def test_ue8m0_sf_bytes(fp8blk):
+    L = fp8blk._L()
+    assert L.fp8blk_ue8m0_sf_bytes(1, 128) == 512
+    assert L.fp8blk_ue8m0_sf_bytes(128, 128) == 512
+    assert L.fp8blk_ue8m0_sf_bytes(129, 384) == 2 * 3 * 512
+    assert L.fp8blk_ue8m0_sf_bytes(4096, 7168) == 32 * 56 * 512
+    assert L.fp8blk_ue8m0_sf_bytes(0, 512) == 0
+    assert L.fp8blk_ue8m0_sf_bytes(5, 0) == 0
+    assert L.fp8blk_ue8m0_sf_bytes(-1, 128) == -1
+    assert L.fp8blk_ue8m0_sf_bytes(16, 96) == -1
+    assert L.fp8blk_ue8m0_sf_bytes(1 << 62, 1 << 20) == -1   # overflow
+
+
+@pytest.mark.parametrize("rows,K", [(1, 128), (128, 256), (200, 384), (300, 1024)])
+def test_ue8m0_tiled_layout_helpers(fp8blk, rows, K):
+    """The binding's layout helpers against the byte offset stated for the
+    tiled scale layout, written out element by element."""
+    import torch
+    rng = np.random.default_rng(rows + K)
+    e = rng.integers(0, 255, size=(rows, K // 32), dtype=np.uint8)
+    sf = fp8blk.ue8m0_sf_from_rows(torch.from_numpy(e), pad=0xEE).numpy()
+    R, KB = (rows + 127) // 128, K // 128
+    assert sf.size == R * KB * 512 == fp8blk.fp8blk_ue8m0_sf_bytes(rows, K)
+    expect = np.full(sf.size, 0xEE, dtype=np.uint8)
+    for r in range(rows):
+        for g in range(K // 32):
+            expect[((r // 128) * KB + g // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + g % 4] = e[r, g]
+    assert np.array_equal(sf, expect)
+    back = fp8blk.ue8m0_sf_to_rows(torch.from_numpy(sf), rows, K).numpy()
+    assert np.array_equal(back, e)
 
 
 def test_linear_fused_rule(fp8blk):

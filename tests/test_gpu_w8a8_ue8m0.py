@@ -14,14 +14,20 @@ pytestmark = pytest.mark.gpu
 
 
 def gpu_quant(x_bits, ldx_pad=0):
+    """Codes [M, K] and exponent bytes [K/32, M] (the oracle's orientation),
+    read back from the tiled scale layout; the padding rows of the last
+    128-row block must hold 127."""
     import block_scaled_fp8_bf16_gb300 as fp8blk
     M, K = x_bits.shape
     xf = np.zeros((M, K + ldx_pad), dtype=np.uint16)
     xf[:, :K] = x_bits
     x = to_dev_bf16(xf)[:, :K]
-    a, e = fp8blk.quant_act_ue8m0(x)
+    a, sf = fp8blk.quant_act_ue8m0(x)
     torch.cuda.synchronize()
-    return a.cpu().numpy(), e[:, :M].cpu().numpy()
+    assert sf.numel() == fp8blk.fp8blk_ue8m0_sf_bytes(M, K)
+    rows = fp8blk.ue8m0_sf_to_rows(sf.cpu(), (M + 127) // 128 * 128, K).numpy()
+    assert np.all(rows[M:] == 127)
+    return a.cpu().numpy(), np.ascontiguousarray(rows[:M].T)
 
 
 @pytest.mark.parametrize("amax_bits", [0x3F80, 0x43E0, 0x43E1, 0x40F0, 0x7F7F, 0x0080, 0x0003, 0x3C01])
@@ -60,20 +66,37 @@ def ue8m0_w8a8_inputs(seed, M, N, K):
 
 
 def gpu_gemm(a, ea, b, eb, f32=False, ldc_pad=0):
+    """The product on the device; ea [K/32, M] as the oracle holds it, tiled
+    on the host with the NaN byte in the padding rows (they only feed rows
+    past M, which are never stored); the weight exponents tiled on the
+    device."""
     import block_scaled_fp8_bf16_gb300 as fp8blk
     M, K = a.shape
     N = b.shape[0]
-    lde = fp8blk.act_exps_pitch(M)
-    e = np.full((K // 32, lde), 0xFF, dtype=np.uint8)             # padding columns: the NaN byte, never read as a scale
-    e[:, :M] = ea
+    a_sf = fp8blk.ue8m0_sf_from_rows(torch.from_numpy(np.ascontiguousarray(ea.T)), pad=0xFF).cuda()
+    b_sf = fp8blk.ue8m0_weight_sf(to_dev(eb))
     c = torch.full((M, N + ldc_pad), 7.0, dtype=torch.float32 if f32 else torch.bfloat16, device="cuda")
-    fp8blk.fp8blk_gemm_w8a8_ue8m0(to_dev(a), to_dev(e), to_dev(b), to_dev(eb), c[:, :N])
+    fp8blk.fp8blk_gemm_w8a8_ue8m0(to_dev(a), a_sf, to_dev(b), b_sf, c[:, :N])
     torch.cuda.synchronize()
     assert fp8blk.fp8blk_device_error() == 0
     out = c.float().cpu().numpy().astype(np.float64)
     if ldc_pad:
         assert np.all(out[:, N:] == 7.0)
     return out[:, :N]
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (384, 1024), (7168, 2048), (2048, 7168), (256, 384)])
+def test_weight_sf_is_the_block_exponents_per_column(lib, N, K):
+    """fp8blk_ue8m0_weight_sf writes block (n/32, g)'s byte for every column
+    n of the block, in the tiled layout, bit for bit."""
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    _, eb = synth.ue8m0_weights(N + K, N, K)
+    sf = fp8blk.ue8m0_weight_sf(to_dev(eb)).cpu()
+    torch.cuda.synchronize()
+    assert sf.numel() == fp8blk.fp8blk_ue8m0_sf_bytes(N, K)
+    per_column = np.repeat(eb, 32, axis=0)                          # [N, K/32]
+    assert np.array_equal(fp8blk.ue8m0_sf_to_rows(sf, N, K).numpy(), per_column)
+    assert torch.equal(sf, fp8blk.ue8m0_sf_from_rows(torch.from_numpy(per_column)))
 
 
 @pytest.mark.parametrize("M,N,K", [
@@ -125,13 +148,13 @@ def test_linear_ue8m0_full_size_sampled(lib):
     M, N, K = 4096, 7168, 2048
     x = synth.activations(4, M, K)
     b, eb = synth.ue8m0_weights(4, N, K)
-    a, e = fp8blk.quant_act_ue8m0(to_dev_bf16(x))
-    c = fp8blk.gemm_w8a8_ue8m0(a, e, to_dev(b), to_dev(eb))
+    a, sf = fp8blk.quant_act_ue8m0(to_dev_bf16(x))
+    c = fp8blk.gemm_w8a8_ue8m0(a, sf, to_dev(b), fp8blk.ue8m0_weight_sf(to_dev(eb)))
     torch.cuda.synchronize()
     assert fp8blk.fp8blk_device_error() == 0
     rows = synth.sample_rows(4, M, 32)
     a_ref, ea_ref = O.quant_act_1x32_ue8m0(x[rows])
     assert np.array_equal(a[rows].cpu().numpy(), a_ref)
-    assert np.array_equal(e[:, rows].cpu().numpy(), ea_ref)
+    assert np.array_equal(fp8blk.ue8m0_sf_to_rows(sf.cpu(), M, K).numpy()[rows].T, ea_ref)
     ref = O.gemm_w8a8_ue8m0(a_ref, ea_ref, b, eb)
     assert_gemm_close(bf16_out_to_f64(c)[rows], ref, "w8a8 ue8m0 4096x7168x2048 sampled")
