@@ -450,6 +450,8 @@ fp8blk_status fp8blk_gemm_w8a8_ue8m0(const void* a_e4m3, int64_t lda, const uint
   if (st != FP8BLK_OK) return st;
   p.a_sf = a_sf;
   p.b_sf = b_sf;
+  p.C = c;
+  p.ldc = ldc;
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);

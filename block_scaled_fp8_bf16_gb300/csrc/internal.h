@@ -129,6 +129,8 @@ struct GemmW8A8MxArgs {
   CUtensorMap tmC;    // C [M, N], box {128 bytes of N, 32 (M)}, 128B swizzle
   const uint8_t* a_sf;  // activation exponent bytes, tiled scale layout (rows padded to 128)
   const uint8_t* b_sf;  // weight exponent bytes per column, tiled scale layout
+  void* C;              // C itself, for the split-K form's direct stores
+  int64_t ldc;
   int M, N, K;
   bool pdl;
   bool out_f32;
