@@ -44,7 +44,9 @@
 // tile; negative for a padding tile, which is skipped and left untouched).
 // Tile (mt, nt) then multiplies with rows g*N + nt*128 of the stacked
 // weights [G*N, K] and scales Bs[g][nt][kb]; every role reads the tile's
-// group from row_group and skips the same tiles.
+// group from row_group and skips the same tiles.  Grouped problems whose
+// groups average at least 256 rows run on the CTA-pair kernel instead
+// (gemm_w8a8_pair.cu).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -655,13 +657,18 @@ cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStre
 }  // namespace
 
 cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
-  // Enough 256x256 tiles to keep most CTA pairs busy: the pair kernel
-  // (ungrouped problems only).
+  // Enough 256x256 tiles to keep most CTA pairs busy: the pair kernel.
+  // Grouped problems go there too when the groups average at least 256 rows:
+  // it runs a pair tile once per group among its two 128-row halves, so
+  // 128-row groups would double its work (measured: G = 8 x 512 rows, N = K =
+  // 4096: 72 against 113 us single-CTA; G = 32 x 256 rows: 128 against 187 us;
+  // G = 64 x 128 rows: 225 against 217 us).
   if (p.fused) {
     if (p.M > kFusedMaxM || p.row_group != nullptr) return cudaErrorInvalidValue;
     return p.out_f32 ? launch_single<float, true>(p, dev, stream) : launch_single<__nv_bfloat16, true>(p, dev, stream);
   }
-  if (p.row_group == nullptr && p.M > kW8A8TileM && 2 * w8a8_pair_tiles(p.M, p.N) >= dev.num_sms / 2)
+  const bool pair_groups = p.row_group == nullptr || int64_t(p.M) >= 256 * int64_t(p.groups);
+  if (pair_groups && p.M > kW8A8TileM && 2 * w8a8_pair_tiles(p.M, p.N) >= dev.num_sms / 2)
     return launch_gemm_w8a8_pair(p, dev, stream);
   return p.out_f32 ? launch_single<float, false>(p, dev, stream) : launch_single<__nv_bfloat16, false>(p, dev, stream);
 }

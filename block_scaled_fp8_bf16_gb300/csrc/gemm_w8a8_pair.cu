@@ -37,6 +37,16 @@
 // A last round that would leave at most half of the pairs busy runs its
 // tiles as 256 x 128 halves instead (MMA N = 128), so that it takes about
 // half as long.
+//
+// Grouped (mixture-of-experts) form, row_group != nullptr: the rows of A and
+// C come in 128-row tiles of one group each (row_group[m] names row m's
+// group, negative for padding), and the weights are stacked [G*N, K] with
+// scales [G][N/128][K/128].  Both CTAs of a pair share one B tile, so a pair
+// tile runs once per distinct group among its two 128-row halves: pass 0
+// with the first half's group, pass 1 with the second half's when it
+// differs; a CTA stores its rows only in the pass of its own group, and
+// padding halves are never stored.  The pass-0 items of all tiles come
+// before the pass-1 items, so that the pairs share the real work evenly.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -100,7 +110,7 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
   nt = r / gsz;
 }
 
-// Work items of the persistent loop.  When the tiles leave a last round that
+// Work items of the persistent loop (dense problems).  When the tiles leave a last round that
 // would keep at most half of the pairs busy, each of those last tiles runs as
 // two 256 x 128 halves on two pairs (MMA N = 128), which halves the length of
 // that round.  Items [0, full_items) are whole tiles; item full_items + 2u + h
@@ -108,14 +118,19 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
 struct Items {
   int full_items, num_items;
 };
-__device__ __forceinline__ Items make_items(int num_tiles, int num_pairs) {
+__device__ __forceinline__ Items make_items(int num_tiles, int num_pairs, bool grouped) {
+  if (grouped) return Items{2 * num_tiles, 2 * num_tiles};   // two passes per tile, no half tiles
   const int rem = num_tiles % num_pairs;
   const int split = (num_tiles > num_pairs && rem > 0 && 2 * rem <= num_pairs) ? rem : 0;
   return Items{num_tiles - split, num_tiles + split};
 }
-__device__ __forceinline__ void item_coords(int t, const Items& items, int m_tiles, int n_tiles, int& mt, int& nt,
-                                            int& half) {
-  if (t < items.full_items) {
+__device__ __forceinline__ void item_coords(int t, const Items& items, int m_tiles, int n_tiles, bool grouped,
+                                            int& mt, int& nt, int& half) {
+  if (grouped) {
+    // item t is pass t / num_tiles of tile t % num_tiles
+    tile_coords(t % (m_tiles * n_tiles), m_tiles, n_tiles, mt, nt);
+    half = -1;
+  } else if (t < items.full_items) {
     tile_coords(t, m_tiles, n_tiles, mt, nt);
     half = -1;
   } else {
@@ -128,6 +143,23 @@ __device__ __forceinline__ void item_coords(int t, const Items& items, int m_til
 __device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, int site) {
   *abort_flag = 1;
   atomicCAS(err, 0, kDevErrW8A8 | 0x80 | site);
+}
+
+// Group of the 128 rows starting at row r (-1 past M: padding).
+__device__ __forceinline__ int half_group(const int* row_group, int r, int M) {
+  return r < M ? __ldg(row_group + r) : -1;
+}
+
+// Grouped: the group that item t's pass multiplies with (pass t / num_tiles
+// of pair tile row mt), or -1 when the pass has no rows to compute (padding,
+// a second half of the same group, or a group past the weights).  Dense
+// problems: 0.
+__device__ __forceinline__ int item_group(const int* row_group, int G, int M, int t, int num_tiles, int mt) {
+  if (row_group == nullptr) return 0;
+  const int g0 = half_group(row_group, mt * 2 * TM, M);
+  const int g1 = half_group(row_group, mt * 2 * TM + TM, M);
+  const int g = t < num_tiles ? g0 : (g1 != g0 ? g1 : -1);
+  return g < G ? g : -1;
 }
 
 // try_wait with cluster-scope acquire, for phases completed by the peer CTA.
@@ -177,7 +209,8 @@ template <bool F32>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmAsG, const __grid_constant__ CUtensorMap tmC,
-                     const float* __restrict__ Bs, int M, int N, int K, int* __restrict__ err) {
+                     const float* __restrict__ Bs, const int* __restrict__ row_group, int G, int M, int N, int K,
+                     int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -206,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tiles = (M + 2 * TM - 1) / (2 * TM);
   const int n_tiles = (N + PN - 1) / PN;
   const int num_tiles = m_tiles * n_tiles;
-  const Items items = make_items(num_tiles, num_pairs);
+  const Items items = make_items(num_tiles, num_pairs, row_group != nullptr);
   const int kblocks = K / BK;
 
   if (threadIdx.x == 0) {
@@ -259,11 +292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = pair; t < items.num_items && ok; t += num_pairs) {
         int mt, nt, half;
-        item_coords(t, items, m_tiles, n_tiles, mt, nt, half);
+        item_coords(t, items, m_tiles, n_tiles, row_group != nullptr, mt, nt, half);
+        const int g = item_group(row_group, G, M, t, num_tiles, mt);
+        if (g < 0) continue;
         const int m0 = mt * 2 * TM + rank * TM;
         // A half tile's MMA reads the first 64 of this CTA's B rows: rows
         // 128 half + 64 rank of the tile (the box's other 64 rows go unused).
-        const int n0 = half < 0 ? nt * PN + rank * HN : nt * PN + half * HN + rank * (HN / 2);
+        // Grouped: group g's weights are rows g*N .. g*N + N - 1.
+        const int n0 = g * N + (half < 0 ? nt * PN + rank * HN : nt * PN + half * HN + rank * (HN / 2));
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
@@ -321,6 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int t = pair; t < items.num_items && ok; t += num_pairs) {
+        if (row_group != nullptr) {
+          int mt, nt, half;
+          item_coords(t, items, m_tiles, n_tiles, true, mt, nt, half);
+          if (item_group(row_group, G, M, t, num_tiles, mt) < 0) continue;
+        }
         const uint32_t idesc = t < items.full_items ? kIdesc : kIdescHalf;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           if ((it & 1u) != w) continue;
@@ -371,14 +412,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // whole-tile path keeps its column offsets as constants.
     // y: first row of this warp's 32-row block; n_item: first output column
     // of the tile or half tile.
-    auto promote = [&](auto nc_tag, int y, int n_item) {
+    auto promote = [&](auto nc_tag, int y, int n_item, int g, bool store) {
       constexpr int NC = decltype(nc_tag)::value;
       const int col0 = (e >> 2) * NC;
       const int n = n_item + col0;
       const bool col_ok = n < N;
 #pragma unroll
       for (int j = 0; j < NC / 2; ++j) acc[j] = make_float2(0.f, 0.f);
-      const float* bs_row = Bs + size_t(col_ok ? n / 128 : 0) * kblocks;
+      const float* bs_row = Bs + (size_t(g) * (N / 128) + size_t(col_ok ? n / 128 : 0)) * kblocks;
       float bs_win = 0.f;
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         if ((kb & 31) == 0) bs_win = (col_ok && kb + lane < kblocks) ? __ldg(bs_row + kb + lane) : 0.f;
@@ -427,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (y < M && col_ok) {
+      if (y < M && col_ok && store) {
         // The warp's 32 x NC block leaves as 128-byte-wide boxes (64 bf16 or
         // 32 float32 columns), at most kBoxesPerWarp at a time through the
         // staging boxes; chunk c (16 bytes) of row r sits at 16-byte
@@ -460,12 +501,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Items it_sh{items_sh[0], items_sh[1]};
       if (t >= it_sh.num_items) break;
       int mt, nt, half;
-      item_coords(t, it_sh, m_tiles, n_tiles, mt, nt, half);
+      item_coords(t, it_sh, m_tiles, n_tiles, row_group != nullptr, mt, nt, half);
+      const int g = item_group(row_group, G, M, t, num_tiles, mt);
+      if (g < 0) {
+        // A group index past the weights in this CTA's rows: skipped and
+        // reported (by one thread).
+        if (row_group != nullptr && threadIdx.x == 128) {
+          const int own = half_group(row_group, mt * 2 * TM + rank * TM, M);
+          if (own >= G) atomicCAS(err, 0, kDevErrW8A8 | kSiteBadGroup);
+        }
+        continue;
+      }
+      // Grouped: this CTA's rows are stored in the pass of their own group.
+      const bool store = row_group == nullptr || half_group(row_group, mt * 2 * TM + rank * TM, M) == g;
       const int y = mt * 2 * TM + rank * TM + quarter * 32;
       if (half < 0)
-        promote(std::integral_constant<int, kCols>{}, y, nt * PN);
+        promote(std::integral_constant<int, kCols>{}, y, nt * PN, g, store);
       else
-        promote(std::integral_constant<int, kCols / 2>{}, y, nt * PN + half * HN);
+        promote(std::integral_constant<int, kCols / 2>{}, y, nt * PN + half * HN, g, store);
     }
     if (lane == 0) bulk_wait_group0();   // the staging buffer stays valid until the stores are done
   }
@@ -522,7 +575,8 @@ cudaError_t launch_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel<F32>, p.tmA, p.tmB, p.tmAsG, p.tmC, p.Bs, p.M, p.N, p.K, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel<F32>, p.tmA, p.tmB, p.tmAsG, p.tmC, p.Bs, p.row_group, p.groups, p.M,
+                            p.N, p.K, p.err);
 }
 
 }  // namespace

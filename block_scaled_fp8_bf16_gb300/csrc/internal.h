@@ -108,8 +108,8 @@ int w8a8_pair_tiles(int M, int N);
 cudaError_t launch_gemm_w8a8_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t s);
 
 // ------------------------------------------------------------------ W8A8, 32x32 UE8M0 format
-// Activation quantiser with power-of-two 1x32 scales (exponent bytes
-// [K/32][lde], M contiguous) and the block-scaled tensor-core product.
+// Activation quantiser with power-of-two 1x32 scales (exponent bytes in the
+// tiled scale layout) and the block-scaled tensor-core product.
 struct QuantActUe8m0Args {
   const void* x;      // bf16 [M, K] pitch ldx
   int64_t ldx;

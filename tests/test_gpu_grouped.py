@@ -50,6 +50,12 @@ def run_grouped(lib, a, As, b, Bs, row_group, dtype=torch.bfloat16):
     ((3, 2), 512, 256, (2,), torch.float32),                # float32 output
     ((1,), 128, 128, (), torch.bfloat16),                   # one group, one tile, one K block
     ((6, 5, 7, 4, 8, 2, 3, 5), 1024, 1024, (9, 20), torch.bfloat16),   # more tiles than one wave
+    # CTA-pair path (enough 256 x 256 tiles): groups not aligned to 256 rows,
+    # so many pair tiles hold two groups (two passes), padding halves, and
+    # one group of 256-row multiples
+    ((3, 4, 1, 6, 2), 2048, 512, (0, 7), torch.float32),
+    ((4, 2, 6), 4096, 384, (), torch.bfloat16),
+    ((1, 3, 2, 5, 1, 4), 2048, 1024, (1, 12), torch.bfloat16),
 ])
 def test_grouped_matches_oracle(lib, tiles, N, K, pads, dtype):
     a, As, b, Bs, g = grouped_inputs(sum(tiles) + N + K, tiles, N, K, pads)
@@ -62,16 +68,22 @@ def test_grouped_matches_oracle(lib, tiles, N, K, pads, dtype):
     assert np.all(out[~real] == 7.0)
 
 
-def test_grouped_out_of_range_group_is_skipped_and_reported(lib):
-    a, As, b, Bs, g = grouped_inputs(3, (1, 2), 256, 256)
+@pytest.mark.parametrize("tiles,N,bad", [
+    ((1, 2), 256, 1),        # single-CTA path
+    ((5, 6), 2048, 3),       # CTA-pair path: the second half of a pair tile
+    ((5, 6), 2048, 4),       # CTA-pair path: the first half of a pair tile
+])
+def test_grouped_out_of_range_group_is_skipped_and_reported(lib, tiles, N, bad):
+    a, As, b, Bs, g = grouped_inputs(3, tiles, N, 256)
     g = g.copy()
-    g[128:256] = 5                                  # tile 1 names a group past the 2 expert weights
+    r0 = 128 * bad
+    g[r0:r0 + 128] = 5                              # this tile names a group past the expert weights
     lib.fp8blk_device_error(clear=True)
     out = run_grouped(lib, a, As, b, Bs, g)
     code = lib.fp8blk_device_error(clear=True)
     assert code == 0x100 | 11
     good = np.ones(g.size, dtype=bool)
-    good[128:256] = False
+    good[r0:r0 + 128] = False
     ref = O.gemm_w8a8_grouped(a, As, b, Bs, np.where(good, g, -1))
     assert_gemm_close(out[good], ref[good], "grouped with a bad tile")
     assert np.all(out[~good] == 7.0)
