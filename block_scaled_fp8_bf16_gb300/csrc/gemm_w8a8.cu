@@ -668,8 +668,15 @@ cudaError_t launch_gemm_w8a8(const GemmW8A8Args& p, const DeviceInfo& dev, cudaS
     return p.out_f32 ? launch_single<float, true>(p, dev, stream) : launch_single<__nv_bfloat16, true>(p, dev, stream);
   }
   const bool pair_groups = p.row_group == nullptr || int64_t(p.M) >= 256 * int64_t(p.groups);
-  if (pair_groups && p.M > kW8A8TileM && 2 * w8a8_pair_tiles(p.M, p.N) >= dev.num_sms / 2)
-    return launch_gemm_w8a8_pair(p, dev, stream);
+  const int pair_tiles = w8a8_pair_tiles(p.M, p.N);
+  const bool pair_whole = 2 * pair_tiles >= dev.num_sms / 2;
+  // Few pair tiles, but more 128 x 128 tiles than the single-CTA kernel can
+  // split over K (M = 256, N = 7168: 112 tiles): the pair kernel runs every
+  // tile as two 256 x 128 halves, whose MMAs do twice the single-CTA work per
+  // SM and cycle (measured: M = 256, N = 7168, K = 18432: 80.7 us single-CTA).
+  const int single_tiles = (p.M + kW8A8TileM - 1) / kW8A8TileM * (p.N / kW8A8TileN);
+  const bool pair_halves = p.row_group == nullptr && 4 * pair_tiles <= dev.num_sms && 2 * single_tiles > dev.num_sms;
+  if (pair_groups && p.M > kW8A8TileM && (pair_whole || pair_halves)) return launch_gemm_w8a8_pair(p, dev, stream);
   return p.out_f32 ? launch_single<float, false>(p, dev, stream) : launch_single<__nv_bfloat16, false>(p, dev, stream);
 }
 

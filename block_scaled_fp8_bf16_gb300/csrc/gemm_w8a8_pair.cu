@@ -110,16 +110,19 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
   nt = r / gsz;
 }
 
-// Work items of the persistent loop (dense problems).  When the tiles leave a last round that
-// would keep at most half of the pairs busy, each of those last tiles runs as
-// two 256 x 128 halves on two pairs (MMA N = 128), which halves the length of
-// that round.  Items [0, full_items) are whole tiles; item full_items + 2u + h
-// is half h of tile full_items + u.  half = -1 marks a whole tile.
+// Work items of the persistent loop (dense problems).  When the tiles leave a
+// last round that would keep at most half of the pairs busy, each of those
+// last tiles runs as two 256 x 128 halves on two pairs (MMA N = 128), which
+// halves the length of that round; when all tiles fit on half of the pairs
+// (the launch then gives two pairs per tile), every tile runs as two halves.
+// Items [0, full_items) are whole tiles; item full_items + 2u + h is half h
+// of tile full_items + u.  half = -1 marks a whole tile.
 struct Items {
   int full_items, num_items;
 };
 __device__ __forceinline__ Items make_items(int num_tiles, int num_pairs, bool grouped) {
   if (grouped) return Items{2 * num_tiles, 2 * num_tiles};   // two passes per tile, no half tiles
+  if (2 * num_tiles <= num_pairs) return Items{0, 2 * num_tiles};
   const int rem = num_tiles % num_pairs;
   const int split = (num_tiles > num_pairs && rem > 0 && 2 * rem <= num_pairs) ? rem : 0;
   return Items{num_tiles - split, num_tiles + split};
@@ -560,7 +563,10 @@ cudaError_t launch_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream
   }
   const int tiles = w8a8_pair_tiles(p.M, p.N);
   const int max_pairs = dev.num_sms / 2;
-  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  // Dense problems whose tiles fit on half of the pairs run every tile as two
+  // 256 x 128 halves, one pair each (see make_items).
+  const int items = (p.row_group == nullptr && 2 * tiles <= max_pairs) ? 2 * tiles : tiles;
+  const int pairs = items < max_pairs ? items : max_pairs;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(2 * pairs), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

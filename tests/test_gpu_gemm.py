@@ -52,6 +52,9 @@ def gpu_w8a8(a, As, b, Bs, ldc_pad=0, lds_pad=0):
     (1000, 2432, 1024),    # CTA-pair path, 40 tiles (no split last round)
     (513, 8192, 384),      # CTA-pair path, one row past a tile boundary; 96 tiles: last 20 split in halves
     (2304, 2304, 256),     # CTA-pair path, 81 tiles: the last 5 run as 10 half tiles
+    (256, 7168, 512),      # CTA-pair path, 28 tiles all run as 56 half tiles (too many 128 x 128 tiles to split K)
+    (200, 6144, 384),      # all halves, ragged second CTA of every pair
+    (130, 4992, 256),      # all halves, the last tile's second half lies wholly past N
 ])
 def test_w8a8_matches_oracle(lib, M, N, K):
     a, As, b, Bs = w8a8_inputs(M + N + K, M, N, K)
