@@ -448,6 +448,13 @@ fp8blk_status fp8blk_gemm_w8a8_ue8m0(const void* a_e4m3, int64_t lda, const uint
   else
     st = make_map(p.tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c, uint64_t(N), uint64_t(M), uint64_t(ldc) * 2, 64, 32);
   if (st != FP8BLK_OK) return st;
+  // The tiled scale arrays as rows of 128 words (one 512-byte block per row).
+  st = make_map(p.tmSfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, a_sf, 128, uint64_t((M + 127) / 128) * uint64_t(K / 128),
+                512, 128, 1, false);
+  if (st != FP8BLK_OK) return st;
+  st = make_map(p.tmSfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, b_sf, 128, uint64_t(N / 128) * uint64_t(K / 128), 512, 128,
+                1, false);
+  if (st != FP8BLK_OK) return st;
   p.a_sf = a_sf;
   p.b_sf = b_sf;
   p.C = c;

@@ -42,10 +42,13 @@
 //               B columns 0..127 and 128..255) into a 4-stage ring, one
 //               barrier per stage.
 //   warp 1      TMEM allocation (512 columns: the 256-column accumulator and
-//               four scale slots of 12 columns); one thread copies the
-//               stage's scale blocks into its TMEM slot with tcgen05.cp and
-//               issues the four K = 32 MMAs of the block (scale byte j for
-//               slice j); the copies and the MMAs of one thread run in order.
+//               four scale slots of 12 columns).
+//   warps 1, 2  one thread each takes alternate K blocks: it copies the
+//               stage's scale blocks into the block's TMEM slot with
+//               tcgen05.cp and issues the four K = 32 MMAs (scale byte j for
+//               slice j); the two take turns through a barrier pair, so the
+//               blocks reach the accumulator in order, and each commits its
+//               own stages.
 //   warps 4..7  epilogue: the accumulator rows of their lane quarter into
 //               registers (bf16), the accumulator released for the next tile,
 //               then TMA tensor stores from a swizzled staging box while the
@@ -246,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + kStages;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* turn = drain + 1;   // [2]: issuer w may issue its next K block
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(turn + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   griddep_launch_dependents();
@@ -269,9 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);    // producer, with the bytes
       mbar_init(&empty[s], 1);   // MMA commit
     }
-    mbar_init(acc_full, 1);
+    mbar_init(acc_full, 2);      // both issuers' commits
     mbar_init(acc_empty, 4);     // the four epilogue warps
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
+    mbar_init(&turn[0], 1);
+    mbar_init(&turn[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -327,19 +333,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0u;
         for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1u, nullptr);
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if ((warp == 1 || warp == 2) && lane == 0) {
+      // ---------------------------------------------------------- MMA issuers
+      // Issuer w (warps 1 and 2) takes the K blocks `it` with it % 2 == w.
+      // One issuing thread alone leaves the tensor pipe idle while it waits
+      // on its barrier and commits (the pipe takes an MMA only as the
+      // previous one finishes); two issuers hide that.  They take turns
+      // through turn[]: block it is issued only after block it - 1 (the
+      // fences order the other thread's MMAs before this thread's), so the
+      // accumulator sees the blocks in order.
+      const uint32_t w = uint32_t(warp - 1);
       uint32_t it = 0;
       bool ok = true;
       int i = 0;
       for (int t = tile0; t < num_tiles && ok; t += tile_step, ++i) {
-        if (!mbar_wait(acc_empty, (uint32_t(i) & 1u) ^ 1u, abort_flag)) {
-          raise_error(err, abort_flag, kSiteMmaAccEmpty);
-          break;
-        }
-        tc_fence_after();
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          if ((it & 1u) != w) continue;
           const int s = int(it % kStages);
+          if (kb == kb0 && !mbar_wait(acc_empty, (uint32_t(i) & 1u) ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaAccEmpty);
+            ok = false;
+            break;
+          }
           if (!mbar_wait(&full[s], (it / kStages) & 1u, abort_flag)) {
             raise_error(err, abort_flag, kSiteMmaFull);
             ok = false;
@@ -354,13 +369,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_cp_sf(sfa, sf_desc(sfs));
           tmem_cp_sf(sfb, sf_desc(sfs + 512u));
           tmem_cp_sf(sfb + 4u, sf_desc(sfs + 1024u));
+          // Turn: issuer 0's k-th block waits for the k-th arrival of issuer
+          // 1 (none for its first), issuer 1's k-th for the (k + 1)-th.
+          const uint32_t k = it >> 1;
+          if ((w == 1u || k > 0u) && !mbar_wait(&turn[w], w == 0u ? ((k - 1u) & 1u) : (k & 1u), abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaFull);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int j = 0; j < BK / 32; ++j)
             mma_mx(tmem, desc_sw128_kmajor(a0 + 32u * j), desc_sw128_kmajor(b0 + 32u * j),
                    mx_idesc(BM, BN, uint32_t(j)), sfa, sfb, (kb > kb0 || j > 0) ? 1u : 0u);
+          tc_fence_before();
+          mbar_arrive(&turn[w ^ 1u]);
           mma_commit(&empty[s]);
         }
-        if (ok) mma_commit(acc_full);
+        if (ok) mma_commit(acc_full);   // each issuer's share of the tile
       }
       // TMEM is released only after every MMA issued above has completed.
       mma_commit(drain);
@@ -538,6 +564,288 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ CTA pairs
+// w8a8_mx_pair_kernel: the same product on CTA pairs (tcgen05 .cta_group::2),
+// 256 x 256 output tiles, for problems with enough tiles to keep most pairs
+// busy.  Each CTA loads its 128 rows of A and its 128 rows of B (N) per K
+// block, so per SM the operand bytes per FLOP are two thirds of the 128 x 256
+// single-CTA tile's; one thread of the even CTA copies the scale blocks into
+// TMEM (tcgen05.cp.cta_group::2: each CTA's own shared memory into its own
+// TMEM) and issues M = 256, N = 256 block-scaled MMAs.  A CTA's scale area
+// holds its own 128 rows' activation scales and the weight scales of all 256
+// columns (both CTAs' MMA halves read every column's scale), loaded with 2-D
+// tensor maps so that blocks past M or N arrive zero-filled.
+//   warp 0      TMA producer (both CTAs; the bytes complete on the even CTA's
+//               stage barrier, whose producer announces the pair's bytes);
+//   warp 1      TMEM allocation with the peer;
+//   warps 1, 2  in the even CTA, one thread each issues the copies and MMAs of
+//               alternate K blocks, taking turns, and multicasts its commits;
+//   warps 4..7  epilogue of the CTA's 128 rows, releasing the accumulator to
+//               the even CTA's issuer before the stores.
+constexpr int PTM = 128;                    // A rows per CTA (256 per pair)
+constexpr int PBN = 256;                    // C columns per pair tile (MMA N)
+constexpr int PHN = PBN / 2;                // B rows per CTA
+constexpr int kPStages = 6;
+constexpr int kPStageA = PTM * BK;
+constexpr int kPStageB = PHN * BK;
+constexpr int kPStageBytes = kPStageA + kPStageB;
+constexpr size_t kPSfOff = size_t(kPStages) * kPStageBytes;
+constexpr size_t kPCOff = kPSfOff + size_t(kPStages) * kSfBytes;
+constexpr size_t kPBarOff = kPCOff + size_t(4) * kStageC;
+constexpr size_t kPSmemBytes = kPBarOff + 256 + 1024;
+static_assert(kSfCols * kPStages + PBN <= int(kTmemCols), "TMEM budget (pair)");
+static_assert(kPSmemBytes <= 232448, "shared memory per CTA (pair)");
+static_assert(kPStageA % 1024 == 0 && kPStageB % 1024 == 0 && kPCOff % 1024 == 0, "swizzle atoms (pair)");
+
+__device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], P;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tmem_cp_sf_pair(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+template <bool F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    w8a8_mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSfa,
+                        const __grid_constant__ CUtensorMap tmSfb, int M, int N, int K, int* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPBarOff);
+  uint64_t* empty = full + kPStages;
+  uint64_t* acc_full = empty + kPStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint64_t* turn = drain + 1;   // [2] (even CTA): issuer w may issue its next K block
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(turn + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = int(cluster_ctarank());
+  const int pair = int(blockIdx.x) >> 1;
+  const int num_pairs = int(gridDim.x) >> 1;
+  const int n_tiles = (N + PBN - 1) / PBN;
+  const int num_tiles = ((M + 2 * PTM - 1) / (2 * PTM)) * n_tiles;
+  const int kblocks = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&full[s], 1);    // the even CTA's producer, with both CTAs' bytes
+      mbar_init(&empty[s], 1);   // MMA commit (multicast to both CTAs)
+    }
+    mbar_init(acc_full, 2);      // both issuers' commits (multicast)
+    mbar_init(acc_empty, 8);     // both CTAs' epilogue warps (used in the even CTA)
+    mbar_init(drain, 2);
+    mbar_init(&turn[0], 1);
+    mbar_init(&turn[1], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmSfa);
+    tma_prefetch_desc(&tmSfb);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // the peer's barriers exist before any commit or arrive reaches them
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t sf_base = tmem + kAccCols;
+
+  if (warp < 4) {
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
+      griddep_wait();   // A and its scales may be the previous kernel's output
+      const uint32_t full0 = map_shared_rank(smem_u32(full), 0);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+        const int mt = t / n_tiles, nt = t - (t / n_tiles) * n_tiles;
+        const int m0 = mt * 2 * PTM + rank * PTM;   // this CTA's A rows
+        const int n0 = nt * PBN;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = int(it % kPStages);
+          if (!mbar_wait(&empty[s], ((it / kPStages) & 1u) ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteProducerEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + size_t(s) * kPStageBytes;
+          uint8_t* sf = smem + kPSfOff + size_t(s) * kSfBytes;
+          const uint32_t bar = full0 + uint32_t(s) * 8u;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (kPStageBytes + kSfBytes));
+          tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
+          tma_load_2d_pair(sa + kPStageA, &tmB, bar, kb * BK, n0 + rank * PHN);
+          // Scale blocks: 512-byte rows of the tiled arrays (128 words each).
+          tma_load_2d_pair(sf, &tmSfa, bar, 0, (m0 / 128) * kblocks + kb);
+          tma_load_2d_pair(sf + 512, &tmSfb, bar, 0, (n0 / 128) * kblocks + kb);
+          tma_load_2d_pair(sf + 1024, &tmSfb, bar, 0, (n0 / 128 + 1) * kblocks + kb);
+        }
+      }
+      if (!ok && rank == 0) {
+        const uint32_t first = it > uint32_t(kPStages) ? it - kPStages : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % kPStages], (j / kPStages) & 1u, nullptr);
+      }
+    } else if ((warp == 1 || warp == 2) && lane == 0 && rank == 0) {
+      // ---------------------------------------------------------- MMA issuers (even CTA)
+      // Two issuers taking turns, as in the single-CTA kernel.
+      const uint32_t w = uint32_t(warp - 1);
+      uint32_t it = 0;
+      bool ok = true;
+      int i = 0;
+      for (int t = pair; t < num_tiles && ok; t += num_pairs, ++i) {
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          if ((it & 1u) != w) continue;
+          const int s = int(it % kPStages);
+          if (kb == 0 && !mbar_wait_acq_cluster(acc_empty, (uint32_t(i) & 1u) ^ 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaAccEmpty);
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_acq_cluster(&full[s], (it / kPStages) & 1u, abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaFull);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + size_t(s) * kPStageBytes);
+          const uint32_t b0 = a0 + kPStageA;
+          const uint32_t sfa = sf_base + uint32_t(s * kSfCols);
+          const uint32_t sfb = sfa + 4u;
+          const uint32_t sfs = smem_u32(smem + kPSfOff + size_t(s) * kSfBytes);
+          tmem_cp_sf_pair(sfa, sf_desc(sfs));
+          tmem_cp_sf_pair(sfb, sf_desc(sfs + 512u));
+          tmem_cp_sf_pair(sfb + 4u, sf_desc(sfs + 1024u));
+          const uint32_t k = it >> 1;
+          if ((w == 1u || k > 0u) && !mbar_wait(&turn[w], w == 0u ? ((k - 1u) & 1u) : (k & 1u), abort_flag)) {
+            raise_error(err, abort_flag, kSiteMmaFull);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int j = 0; j < BK / 32; ++j)
+            mma_mx_pair(tmem, desc_sw128_kmajor(a0 + 32u * j), desc_sw128_kmajor(b0 + 32u * j),
+                        mx_idesc(2 * PTM, PBN, uint32_t(j)), sfa, sfb, (kb > 0 || j > 0) ? 1u : 0u);
+          tc_fence_before();
+          mbar_arrive(&turn[w ^ 1u]);
+          mma_commit_pair_mc(&empty[s], 0x3);
+        }
+        if (ok) mma_commit_pair_mc(acc_full, 0x3);   // each issuer's share of the tile
+      }
+      mma_commit_pair_mc(drain, 0x1);
+      if (!mbar_wait(drain, 0, nullptr)) raise_error(err, abort_flag, kSiteDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const uint32_t lane_base = uint32_t(32 * q) << 16;
+    const uint32_t acc_empty0 = map_shared_rank(smem_u32(acc_empty), 0);
+    uint8_t* box = smem + kPCOff + size_t(q) * kStageC;
+    int i = 0;
+    for (int t = pair; t < num_tiles; t += num_pairs, ++i) {
+      const int mt = t / n_tiles, nt = t - (t / n_tiles) * n_tiles;
+      const int y = mt * 2 * PTM + rank * PTM + 32 * q;   // this warp's first output row
+      const int n0 = nt * PBN;
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_full, uint32_t(i) & 1u, abort_flag))) {
+        raise_error(err, abort_flag, kSiteEpilogueFull);
+        break;
+      }
+      tc_fence_after();
+      const bool rows = y < M;
+      if constexpr (!F32) {
+        uint32_t packed[PBN / 2];
+#pragma unroll
+        for (int c = 0; c < PBN; c += 64) {
+          uint32_t v[64];
+          tmem_ld_x32(tmem + lane_base + uint32_t(c), v);
+          tmem_ld_x32(tmem + lane_base + uint32_t(c + 32), v + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            packed[c / 2 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty0);
+#pragma unroll
+        for (int b = 0; b < PBN / 64; ++b) {
+          if (rows && n0 + 64 * b < N) {
+            if (lane == 0) wait_staging();
+            __syncwarp();
+            uint8_t* dst = box + lane * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(dst + ((ch ^ (lane & 7)) << 4)) =
+                  make_uint4(packed[32 * b + 4 * ch], packed[32 * b + 4 * ch + 1], packed[32 * b + 4 * ch + 2],
+                             packed[32 * b + 4 * ch + 3]);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, box, n0 + 64 * b, y);
+              bulk_commit_group();
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < PBN; c += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem + lane_base + uint32_t(c), v);
+          tmem_ld_wait();
+          if (c + 32 == PBN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty0);
+          }
+          if (rows && n0 + c < N) {
+            if (lane == 0) wait_staging();
+            __syncwarp();
+            uint8_t* dst = box + lane * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(dst + ((ch ^ (lane & 7)) << 4)) =
+                  make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, box, n0 + c, y);
+              bulk_commit_group();
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group0();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // neither CTA leaves while the other may still reach its shared memory or TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_quant_act_ue8m0(const QuantActUe8m0Args& p, const DeviceInfo& dev, cudaStream_t s) {
@@ -615,7 +923,49 @@ cudaError_t launch_mx(const GemmW8A8MxArgs& p, const DeviceInfo& dev, cudaStream
 }
 }  // namespace
 
+namespace {
+template <bool F32>
+cudaError_t launch_mx_pair(const GemmW8A8MxArgs& p, const DeviceInfo& dev, cudaStream_t stream) {
+  static bool attr_done[64] = {};
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if (device < 64 && !attr_done[device]) {
+    e = cudaFuncSetAttribute(w8a8_mx_pair_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kPSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done[device] = true;
+  }
+  const int tiles = mx_pair_tiles(p.M, p.N);
+  const int max_pairs = dev.num_sms / 2;
+  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, w8a8_mx_pair_kernel<F32>, p.tmA, p.tmB, p.tmC, p.tmSfa, p.tmSfb, p.M, p.N, p.K,
+                            p.err);
+}
+}  // namespace
+
+int mx_pair_tiles(int M, int N) { return ((M + 2 * PTM - 1) / (2 * PTM)) * ((N + PBN - 1) / PBN); }
+
 cudaError_t launch_gemm_w8a8_mx(const GemmW8A8MxArgs& p, const DeviceInfo& dev, cudaStream_t s) {
+  // Enough 256 x 256 tiles to keep at least half of the CTA pairs busy: the
+  // pair kernel; otherwise the single-CTA kernel (K split over a cluster
+  // when its tiles leave most SMs idle).
+  if (p.M > PTM && 2 * mx_pair_tiles(p.M, p.N) >= dev.num_sms / 2)
+    return p.out_f32 ? launch_mx_pair<true>(p, dev, s) : launch_mx_pair<false>(p, dev, s);
   return p.out_f32 ? launch_mx<true>(p, dev, s) : launch_mx<false>(p, dev, s);
 }
 

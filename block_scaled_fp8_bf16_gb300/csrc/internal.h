@@ -127,6 +127,8 @@ struct GemmW8A8MxArgs {
   CUtensorMap tmA;    // e4m3 [M, K], box {128 (K), 128 (M)}, 128B swizzle
   CUtensorMap tmB;    // e4m3 [N, K], box {128 (K), 128 (N)}, 128B swizzle
   CUtensorMap tmC;    // C [M, N], box {128 bytes of N, 32 (M)}, 128B swizzle
+  CUtensorMap tmSfa;  // the activation scale array as uint32 [blocks][128], box {128, 1} (pair kernel)
+  CUtensorMap tmSfb;  // the weight scale array, the same way
   const uint8_t* a_sf;  // activation exponent bytes, tiled scale layout (rows padded to 128)
   const uint8_t* b_sf;  // weight exponent bytes per column, tiled scale layout
   void* C;              // C itself, for the split-K form's direct stores
@@ -137,6 +139,7 @@ struct GemmW8A8MxArgs {
   int* err;
 };
 cudaError_t launch_gemm_w8a8_mx(const GemmW8A8MxArgs& p, const DeviceInfo& dev, cudaStream_t s);
+int mx_pair_tiles(int M, int N);
 
 // ------------------------------------------------------------------ W8A16
 struct GemmW8A16Args {

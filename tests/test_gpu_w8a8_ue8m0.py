@@ -106,6 +106,9 @@ def test_weight_sf_is_the_block_exponents_per_column(lib, N, K):
     (200, 2048, 7168),    # the UE8M0 workload's shapes, ragged M
     (300, 7168, 2048),
     (64, 512, 384),       # three K blocks
+    (520, 4992, 384),     # CTA-pair kernel: ragged M (a pair tile's second CTA wholly past M), a last column
+                          # tile of 128 (its second B half and scale block past N)
+    (1024, 4864, 1024),   # CTA-pair kernel, whole tiles
 ])
 def test_gemm_ue8m0_matches_oracle(lib, M, N, K):
     _, a, ea, b, eb = ue8m0_w8a8_inputs(M + N + K, M, N, K)
@@ -113,8 +116,8 @@ def test_gemm_ue8m0_matches_oracle(lib, M, N, K):
     assert_gemm_close(out, O.gemm_w8a8_ue8m0(a, ea, b, eb), f"w8a8 ue8m0 {M}x{N}x{K}")
 
 
-def test_gemm_ue8m0_f32_out_is_unrounded(lib):
-    M, N, K = 130, 512, 1024
+@pytest.mark.parametrize("M,N,K", [(130, 512, 1024), (520, 4992, 384)])
+def test_gemm_ue8m0_f32_out_is_unrounded(lib, M, N, K):
     _, a, ea, b, eb = ue8m0_w8a8_inputs(5, M, N, K)
     ref = O.gemm_w8a8_ue8m0(a, ea, b, eb)
     c32 = gpu_gemm(a, ea, b, eb, f32=True, ldc_pad=4)
@@ -123,19 +126,24 @@ def test_gemm_ue8m0_f32_out_is_unrounded(lib):
     assert np.array_equal(O.bf16_bits_to_f64(O.f64_to_bf16_bits(c32)), c16)
 
 
-def test_gemm_ue8m0_one_hot_rows_exact(lib):
-    """Row i of A holds one 1.0 at column k_i, with its own activation
-    exponent there; C row i is then exactly dec(B[:, k_i]) 2^(ea + eb - 254):
-    this pins which scale byte (block, slice, row, column) the hardware
-    applies to every product."""
-    N, K = 512, 512
+@pytest.mark.parametrize("M,N,rows", [
+    (12, 512, None),                                        # single-CTA kernel: rows 0..11
+    (512, 4864, [0, 37, 127, 128, 200, 255, 256, 300, 383, 384, 450, 511]),   # CTA-pair kernel: rows in both CTAs
+])
+def test_gemm_ue8m0_one_hot_rows_exact(lib, M, N, rows):
+    """Row r of A holds one 1.0 at column k_r, with its own activation
+    exponent there (all other rows zero); C row r is then exactly
+    dec(B[:, k_r]) 2^(ea + eb - 254): this pins which scale byte (block,
+    slice, row, column) the hardware applies to every product, on both
+    kernels (on CTA pairs, rows of the even and of the odd CTA)."""
+    K = 512
     ks = [0, 31, 32, 63, 64, 127, 128, 200, 300, 383, 384, 511]
-    M = len(ks)
+    rows = rows if rows is not None else list(range(M))
     a = np.zeros((M, K), dtype=np.uint8)
     ea = np.full((K // 32, M), 127, dtype=np.uint8)
-    for i, k0 in enumerate(ks):
-        a[i, k0] = 0x38
-        ea[k0 // 32, i] = 127 + (i % 7) - 3
+    for i, (r, k0) in enumerate(zip(rows, ks)):
+        a[r, k0] = 0x38
+        ea[k0 // 32, r] = 127 + (i % 7) - 3
     b, eb = synth.ue8m0_weights(9, N, K)
     out = gpu_gemm(a, ea, b, eb, f32=True)
     assert np.array_equal(out, O.gemm_w8a8_ue8m0(a, ea, b, eb))
