@@ -14,12 +14,17 @@
 //
 //   warp 0      TMA producer: e4m3 weight tile [128 n x 128 k] (16 KB) and
 //               bf16 activation tile [TM x 128 k] per 128-K block.
-//   warp 1      TMEM allocation; one thread issues eight tcgen05.mma
-//               kind::f16 (K = 16) per K block, A from TMEM, B from smem.
-//   warps 2..5  decode: thread = weight row; reads its 128 codes, decodes them
+//   warp 1      TMEM allocation.
+//   warps 1, 2  one thread each issues the eight tcgen05.mma kind::f16
+//               (K = 16) of alternate K blocks, A from TMEM, B from smem (the
+//               tensor pipe takes an MMA only as the previous one finishes, so
+//               one thread alone would leave it idle while it waits and
+//               commits); with UE8M0 scales, whose blocks share one
+//               accumulator, the two take turns through a barrier pair.
+//   warps 3..   decode: thread = weight row; reads its 128 codes, decodes them
 //               exactly to bf16 (integer ops + one packed multiply, see
-//               decode.cuh) and stores them to one of two TMEM A buffers.
-//   warps 6..9  epilogue: thread = weight row n, TM accumulators (tokens).
+//               decode.cuh) and stores them to one of four TMEM A buffers.
+//   then        epilogue: thread = weight row n, TM accumulators (tokens).
 //
 // Scale formats:
 //   fp32 128x128: one FP32 partial per 128-K block in TMEM (double buffered),
@@ -50,6 +55,7 @@ constexpr int kACols = BK / 2;    // TMEM columns of one decoded A block (2 bf16
 constexpr int kABufs = 4;         // decoded A blocks in flight in TMEM
 constexpr int kGroupN = 8;
 constexpr int kBarrierBytes = 512;
+constexpr int kCtlWarps = 3;      // producer, two MMA issuers; the decode warps follow
 
 template <int TM>
 struct Cfg {
@@ -58,10 +64,12 @@ struct Cfg {
   static constexpr int kEpiWarps = TM >= 128 ? 8 : 4;
   static constexpr int kEpiCols = TM / (kEpiWarps / 4);
   // Decode warps: two per TMEM lane quarter (each decodes half of the K
-  // block) unless the epilogue already needs eight warps.
-  static constexpr int kDecWarps = TM >= 64 ? 4 : 8;
+  // block), except at TM = 64, where one per quarter keeps up with the
+  // narrower MMAs (at TM = 128 with two MMA issuers, eight decode warps
+  // measured 3-4 % faster than four).
+  static constexpr int kDecWarps = TM == 64 ? 4 : 8;
   static constexpr int kDecChunks = 8 / (kDecWarps / 4);   // 16-byte chunks of a row per decode warp
-  static constexpr int kThreads = 64 + (kDecWarps + kEpiWarps) * 32;
+  static constexpr int kThreads = 32 * kCtlWarps + (kDecWarps + kEpiWarps) * 32;
   static constexpr int kStageX = TM * BK * 2;                  // bf16 activation tile
   static constexpr int kStageBytes = kStageW + kStageX;
   // One CTA per SM (registers are allocated per 4-warp group, so a second
@@ -126,7 +134,8 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
   uint64_t* dfull = aempty + kABufs;
   uint64_t* dempty = dfull + Q::kDBufs;
   uint64_t* drain = dempty + Q::kDBufs;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* turn = drain + 1;   // [2], UE8M0: issuer w may issue its next K block
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(turn + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   griddep_launch_dependents();   // the next kernel may start its prologue; it gets an SM when this CTA leaves
@@ -154,10 +163,12 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
       mbar_init(&aempty[i], 1);
     }
     for (int i = 0; i < Q::kDBufs; ++i) {
-      mbar_init(&dfull[i], 1);
+      mbar_init(&dfull[i], ue8m0 ? 2 : 1);   // UE8M0: both issuers' commits at the end of a tile
       mbar_init(&dempty[i], Q::kEpiWarps);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
+    mbar_init(&turn[0], 1);
+    mbar_init(&turn[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -180,7 +191,7 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
   float acc[EC];
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;          // weight row within the tile (TMEM lane)
-  const int col0 = warp >= 2 + Q::kDecWarps + 4 ? EC : 0;   // second epilogue warp of a lane quarter
+  const int col0 = warp >= kCtlWarps + Q::kDecWarps + 4 ? EC : 0;   // second epilogue warp of a lane quarter
   int last_nt = 0, last_mt = 0;
 
   if (warp == 0) {
@@ -214,23 +225,32 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
         for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % Q::kStages], (j / Q::kStages) & 1u, nullptr);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // A single thread issues every MMA, so its loop is kept short: ring
-    // positions advance by counters, the stage descriptor is built once per
-    // K block, and the stage's own barrier is not re-tested: "A block
-    // decoded" implies the stage landed, because every decode warp waits for
-    // the stage before it decodes.
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer w takes the K blocks `it` with it % 2 == w, so its stages, A
+    // buffers and (fp32 format) partial buffers are those of its parity; the
+    // stage's own barrier is not re-tested: "A block decoded" implies the
+    // stage landed, because every decode warp waits for the stage before it
+    // decodes.  UE8M0 blocks accumulate into one buffer per tile, so the
+    // issuers take turns there: block it after block it - 1 (the fences
+    // order the other thread's MMAs before this thread's).
     if (lane == 0) {
-      uint32_t s = 0, ph = 0, a = 0, aph = 0, d = 0, dph = 0;
+      const uint32_t w = uint32_t(warp - 1);
+      uint32_t it = 0;
       bool ok = true;
-      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
-        for (int kb = kb_begin; kb < kb_end && ok; ++kb) {
+      int i = 0;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++i) {
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+          if ((it & 1u) != w) continue;
           const bool first_kb = kb == kb_begin;
-          const bool last_kb = kb + 1 == kb_end;
           // fp32 format: one accumulator buffer per K block; UE8M0: per tile.
           const bool new_acc = !ue8m0 || first_kb;
-          const bool done_acc = !ue8m0 || last_kb;
+          const uint32_t acc_it = ue8m0 ? uint32_t(i) : it;
+          const uint32_t d = acc_it % uint32_t(Q::kDBufs);
+          const uint32_t dph = (acc_it / uint32_t(Q::kDBufs)) & 1u;
+          const uint32_t s = it % uint32_t(Q::kStages);
+          const uint32_t a = it % uint32_t(kABufs);
+          const uint32_t aph = (it / uint32_t(kABufs)) & 1u;
           if (new_acc && !mbar_wait(&dempty[d], dph ^ 1u, abort_flag)) {
             raise_error(err, abort_flag, kSiteMmaAccEmpty);
             ok = false;
@@ -240,6 +260,16 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
             raise_error(err, abort_flag, kSiteMmaAFull);
             ok = false;
             break;
+          }
+          if (ue8m0) {
+            // issuer 0's k-th block waits for the k-th arrival of issuer 1
+            // (none for its first), issuer 1's k-th for the (k + 1)-th
+            const uint32_t k = it >> 1;
+            if ((w == 1u || k > 0u) && !mbar_wait(&turn[w], w == 0u ? ((k - 1u) & 1u) : (k & 1u), abort_flag)) {
+              raise_error(err, abort_flag, kSiteMmaAFull);
+              ok = false;
+              break;
+            }
           }
           tc_fence_after();
           const uint64_t xdesc = desc_sw128_kmajor(smem_u32(smem + size_t(s) * Q::kStageBytes + kStageW));
@@ -251,25 +281,25 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
             const uint64_t xd = xdesc + uint64_t(((j >> 2) * TM * 128 + (j & 3) * 32) >> 4);
             mma_bf16_ts(d_tmem, a_tmem + uint32_t(j * 8), xd, Q::kIdesc, (j > 0 || !new_acc) ? 1u : 0u);
           }
+          if (ue8m0) {
+            tc_fence_before();
+            mbar_arrive(&turn[w ^ 1u]);
+          }
           mma_commit(&empty[s]);
           mma_commit(&aempty[a]);
-          if (done_acc) {
-            mma_commit(&dfull[d]);
-            if (++d == uint32_t(Q::kDBufs)) { d = 0; dph ^= 1u; }
-          }
-          if (++s == uint32_t(Q::kStages)) { s = 0; ph ^= 1u; }
-          if (++a == uint32_t(kABufs)) { a = 0; aph ^= 1u; }
+          if (!ue8m0) mma_commit(&dfull[d]);
         }
+        // UE8M0: each issuer's share of the tile's accumulator (count 2).
+        if (ok && ue8m0) mma_commit(&dfull[uint32_t(i) % uint32_t(Q::kDBufs)]);
       }
-      (void)ph;
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else if (warp < 2 + Q::kDecWarps) {
+  } else if (warp < kCtlWarps + Q::kDecWarps) {
     // ------------------------------------------------------------ decode
     // First 16-byte chunk of the row this warp decodes (second warp of a
     // lane quarter takes the upper half of the K block).
-    const int c_first = ((warp - 2) / 4) * Q::kDecChunks;
+    const int c_first = ((warp - kCtlWarps) / 4) * Q::kDecChunks;
     uint32_t it = 0;
     bool ok = true;
     const float* bs32 = static_cast<const float*>(scales);
@@ -400,7 +430,7 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
     // and stores them.  Consecutive threads take consecutive weight rows, so
     // the remote reads and the stores are coalesced and every rank shares
     // the reduction.
-    const bool epi = warp >= 2 + Q::kDecWarps;
+    const bool epi = warp >= kCtlWarps + Q::kDecWarps;
     float* red = reinterpret_cast<float*>(smem);   // [TM][BN] floats, reuses the stages
     if (epi) {
 #pragma unroll
@@ -408,7 +438,7 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
     }
     cluster_sync();
     if (epi && !*abort_flag) {
-      const int et = (warp - 2 - Q::kDecWarps) * 32 + lane;   // 0 .. 32 * kEpiWarps - 1
+      const int et = (warp - kCtlWarps - Q::kDecWarps) * 32 + lane;   // 0 .. 32 * kEpiWarps - 1
       constexpr int kTStep = 32 * Q::kEpiWarps / BN;          // token rows handled per pass
       static_assert(32 * Q::kEpiWarps % BN == 0, "whole token rows per pass");
       const int r_row = et % BN;
