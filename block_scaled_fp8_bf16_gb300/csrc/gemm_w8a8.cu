@@ -88,7 +88,13 @@ template <bool FUSED>
 struct W8A8Cfg {
   static constexpr int kStages = FUSED ? 5 : fp8blk::kStages;
   static constexpr int kQuantWarps = FUSED ? 2 : 0;   // 12 warps: 168 registers per thread
-  static constexpr int kThreads = 64 + (kEpiWarps + kQuantWarps) * 32;
+  // MMA-issuing threads: two on alternate K blocks (the tensor pipe takes an
+  // MMA only as the previous one finishes, so one thread alone leaves it idle
+  // while it waits on its barriers and commits); the fused form keeps one,
+  // since its odd stage count would give one stage to both issuers.
+  static constexpr int kIssuers = FUSED ? 1 : 2;
+  static constexpr int kCtlWarps = 1 + kIssuers;     // producer, issuers; the epilogue warps follow
+  static constexpr int kThreads = 32 * kCtlWarps + (kEpiWarps + kQuantWarps) * 32;
   static constexpr int kStageX = FUSED ? kFusedMaxM * BK * 2 : 0;   // bf16 [32][128] as two 64-column boxes
   static constexpr size_t kAsOff = size_t(kStages) * kStageBytes;
   static constexpr size_t kXOff = (kAsOff + size_t(kStages) * kStageAs + 1023) / 1024 * 1024;
@@ -97,6 +103,8 @@ struct W8A8Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert((3 * kStages + 2 * kAccBufs + 1) * 8 + 8 <= kBarrierBytes, "barrier area");
   static_assert(kFusedMaxM % (4 * (FUSED ? kQuantWarps : 1)) == 0, "whole passes of four rows per quantiser warp");
+  static_assert(kIssuers == 1 || (kStages % 2 == 0 && kAccBufs % 2 == 0),
+                "each stage and partial buffer belongs to one issuer");
 };
 static_assert(W8A8Cfg<false>::kBarOff == size_t(kStages) * (kStageBytes + kStageAs), "unfused layout unchanged");
 
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
       mbar_init(&dfull[d], 1);
       mbar_init(&dempty[d], kEpiWarps);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, Q::kIssuers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
   // reduction after the tile loop.
   float acc[kColsPerThread];
   const int quarter = warp & 3;
-  const int half = (warp - 2) >> 2;
+  const int half = (warp - Q::kCtlWarps) >> 2;
   const int row_in_tile = quarter * 32 + lane;
   int last_mt = 0, last_nt = 0;
 
@@ -311,9 +319,12 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
         for (int j = first; j < it; ++j) mbar_wait(&cbar[j % kStages], (uint32_t(j) / kStages) & 1u, nullptr);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= 1 && warp <= Q::kIssuers) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer w takes the K blocks with it % kIssuers == w, whose stages and
+    // partial buffers are those of its parity.
     if (lane == 0) {
+      const uint32_t w = uint32_t(warp - 1);
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
       for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
@@ -324,6 +335,7 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
           if (g < 0 || g >= G) continue;
         }
         for (int kb = kb_begin; kb < kb_end; ++kb, ++it, ++acc_it) {
+          if (it % uint32_t(Q::kIssuers) != w) continue;
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           const int d = acc_it % kAccBufs;
@@ -355,7 +367,7 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr);
     }
-  } else if (warp < 2 + kEpiWarps) {
+  } else if (warp < Q::kCtlWarps + kEpiWarps) {
     // ------------------------------------------------------------ promotion + epilogue
     griddep_wait();        // the output may still be read or written by the previous kernel
     uint32_t it = 0;       // stage counter, in step with the producer and the MMA issuer
@@ -367,7 +379,7 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
       if (g < 0 || g >= G) {
         // Padding tile, or a group index past the weights: skipped by every
         // role; the latter is also reported in the error word.
-        if (g >= G && threadIdx.x == 64) atomicCAS(err, 0, kDevErrW8A8 | kSiteBadGroup);
+        if (g >= G && threadIdx.x == 32 * Q::kCtlWarps) atomicCAS(err, 0, kDevErrW8A8 | kSiteBadGroup);
         continue;
       }
       last_mt = mt;
@@ -447,7 +459,7 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
     // pass, and the warps interleave: pass j of warp q takes rows
     // 8j + 4q .. 8j + 4q + 3, so both warps work from the fifth row on.  Codes go to the 128-byte-swizzled A tile the MMA
     // reads, one 16-byte chunk per lane and row.
-    const int qw = warp - 2 - kEpiWarps;
+    const int qw = warp - Q::kCtlWarps - kEpiWarps;
     const int sub = lane & 7;              // 16-column slice of the row
     const int rg = lane >> 3;              // row within the pass
     constexpr int kPasses = kFusedMaxM / (4 * Q::kQuantWarps);
@@ -567,7 +579,7 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
     // One tile per cluster: sum the ranks' accumulators through distributed
     // shared memory, in rank order, into rank 0.  Every thread of every CTA
     // reaches both cluster barriers, also after an abort.
-    const bool epi = warp >= 2 && warp < 2 + kEpiWarps;
+    const bool epi = warp >= Q::kCtlWarps && warp < Q::kCtlWarps + kEpiWarps;
     const int m = last_mt * BM + row_in_tile;
     const bool row_ok = epi && m < M;
     float4* red = reinterpret_cast<float4*>(smem);   // [BN/4][BM] float4, reuses stages 0-1
