@@ -38,6 +38,14 @@
 // tiles as 256 x 128 halves instead (MMA N = 128), so that it takes about
 // half as long.
 //
+// Split K (ksplit = 2), for dense problems whose tiles fit on half of the
+// pairs and whose K range is long: a cluster of 4 CTAs (two pairs) per tile,
+// pair p accumulating K blocks [p, p + 1) * kblocks / 2.  At the end the
+// promotion warps of the half of the columns a pair does not keep write
+// their accumulators to shared memory, and after a cluster barrier the
+// keeping warps (pair 0: columns 0..127 of the tile, pair 1: 128..255) add
+// the other pair's values through distributed shared memory and store them.
+//
 // Grouped (mixture-of-experts) form, row_group != nullptr: the rows of A and
 // C come in 128-row tiles of one group each (row_group[m] names row m's
 // group, negative for padding), and the weights are stacked [G*N, K] with
@@ -88,6 +96,10 @@ constexpr uint32_t kIdesc = make_idesc(0 /* e4m3 */, 2 * TM, PN);
 constexpr uint32_t kIdescHalf = make_idesc(0 /* e4m3 */, 2 * TM, HN);   // a 256 x 128 half tile
 constexpr int kGroupM = 8;
 constexpr int kBarrierBytes = 1024;
+// Split K over two pairs from K = 12288: M = 256, N = 7168 took 23.1 / 31.8 /
+// 52.7 us split against 17.8 / 29.9 / 59.9 us as halves at K = 4096 / 8192 /
+// 18432 (the exchange and the four-CTA clusters cost ~6 us up front).
+constexpr int kSplitMinKBlocks = 96;
 constexpr size_t kAsOff = size_t(kStages) * kStageBytes;
 constexpr size_t kCOff = kAsOff + size_t(kAsStages) * kStageAs;   // kEpiWarps staging boxes
 constexpr size_t kBarOff = kCOff + size_t(kEpiWarps) * kBoxesPerWarp * kStageC;
@@ -208,12 +220,13 @@ __device__ __forceinline__ uint4 out_chunk(const float2* acc, int b, int c) {
   return v;
 }
 
-template <bool F32>
+template <bool F32, int ksplit>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmAsG, const __grid_constant__ CUtensorMap tmC,
                      const float* __restrict__ Bs, const int* __restrict__ row_group, int G, int M, int N, int K,
                      int* __restrict__ err) {
+  static_assert(ksplit == 1 || ksplit == 2, "one or two pairs per tile");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -236,14 +249,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rank = static_cast<int>(cluster_ctarank());
-  const int pair = blockIdx.x >> 1;
-  const int num_pairs = gridDim.x >> 1;
+  const int crank = static_cast<int>(cluster_ctarank());
+  const int rank = crank & 1;                            // position in the CTA pair
+  const int even = ksplit == 1 ? 0 : (crank & ~1);       // cluster rank of the pair's even CTA
+  const int kslice = ksplit == 1 ? 0 : (crank >> 1);     // split K: the pair's half of the K blocks
+  const uint16_t pair_mask = uint16_t(0x3u << even);
+  // One slot per pair, or per two pairs with split K (one tile each);
+  // ksplit is 1 or 2, so 2 * ksplit = 1 << ksplit (shifts, not divisions).
+  const int pair = int(blockIdx.x) >> ksplit;
+  const int num_pairs = int(gridDim.x) >> ksplit;
   const int m_tiles = (M + 2 * TM - 1) / (2 * TM);
   const int n_tiles = (N + PN - 1) / PN;
   const int num_tiles = m_tiles * n_tiles;
   const Items items = make_items(num_tiles, num_pairs, row_group != nullptr);
   const int kblocks = K / BK;
+  const int kb0 = kslice * (kblocks >> 1);                  // 0 unless K is split
+  const int kb1 = kslice + 1 == ksplit ? kblocks : (kblocks >> 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -286,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Two issuing threads (A + scales from warp 0, B from warp 2): one thread
     // alone cannot issue strided 128-byte-row tiles at the rate the MMAs use.
     const bool a_side = warp == 0;
-    const uint32_t full0_base = map_shared_rank(smem_u32(full), 0);
+    const uint32_t full0_base = map_shared_rank(smem_u32(full), uint32_t(even));
     if (lane == 0) {
       // Under programmatic dependent launch the weights stream in at once;
       // the activations and their scales wait for the previous kernel.
@@ -303,10 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 128 half + 64 rank of the tile (the box's other 64 rows go unused).
         // Grouped: group g's weights are rows g*N .. g*N + N - 1.
         const int n0 = g * N + (half < 0 ? nt * PN + rank * HN : nt * PN + half * HN + rank * (HN / 2));
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          if (a_side && kb % kAsGroup == 0) {
+          if (a_side && (kb - kb0) % kAsGroup == 0) {
             // Scales of K blocks kb .. kb + kAsGroup - 1 in one box (rows
             // past K / 128 arrive zero-filled and are never read).
             const int j = gi % kAsStages;
@@ -366,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (item_group(row_group, G, M, t, num_tiles, mt) < 0) continue;
         }
         const uint32_t idesc = t < items.full_items ? kIdesc : kIdescHalf;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           if ((it & 1u) != w) continue;
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
@@ -390,11 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f8_ss_pair(d_tmem, desc_sw128_kmajor(a0 + 32u * k), desc_sw128_kmajor(b0 + 32u * k), idesc,
                            k > 0 ? 1u : 0u);
           }
-          mma_commit_pair_mc(&empty[s], 0x3);
-          mma_commit_pair_mc(&dfull[w], 0x3);
+          mma_commit_pair_mc(&empty[s], pair_mask);
+          mma_commit_pair_mc(&dfull[w], pair_mask);
         }
       }
-      mma_commit_pair_mc(drain, 0x1);
+      mma_commit_pair_mc(drain, uint16_t(1u << even));
       mbar_wait(drain, 0, nullptr);
     }
     }
@@ -404,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = warp - 4;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const uint32_t dempty0 = map_shared_rank(smem_u32(dempty), 0);
+    const uint32_t dempty0 = map_shared_rank(smem_u32(dempty), uint32_t(even));
     uint8_t* stg = c_stage + size_t(e) * kBoxesPerWarp * kStageC;
     griddep_wait();   // the output may still be read or written by the previous kernel
     float2 acc[kCols / 2];
@@ -415,6 +436,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // whole-tile path keeps its column offsets as constants.
     // y: first row of this warp's 32-row block; n_item: first output column
     // of the tile or half tile.
+    // The warp's 32 x NC block of acc leaves as 128-byte-wide boxes (64 bf16
+    // or 32 float32 columns), at most kBoxesPerWarp at a time through the
+    // staging boxes; chunk c (16 bytes) of row r sits at 16-byte position
+    // c ^ (r & 7) of the row (128-byte swizzle).  n: first column.
+    auto store_block = [&](auto nc_tag, int y, int n) {
+      constexpr int NC = decltype(nc_tag)::value;
+      constexpr int kBoxCols = F32 ? 32 : 64;
+      constexpr int kBoxes = NC / kBoxCols;
+      constexpr int kPer = kBoxes < kBoxesPerWarp ? kBoxes : kBoxesPerWarp;
+#pragma unroll
+      for (int r = 0; r < kBoxes / kPer; ++r) {
+        if (lane == 0) bulk_wait_group_read0();   // earlier stores have left the staging boxes
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < kPer; ++h) {
+          uint8_t* dst = stg + h * kStageC + lane * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(dst + ((c ^ (lane & 7)) << 4)) = out_chunk<F32>(acc, r * kPer + h, c);
+        }
+        fence_async_shared();   // generic-proxy writes become visible to the TMA engine
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < kPer; ++h) tma_store_2d(&tmC, stg + h * kStageC, n + (r * kPer + h) * kBoxCols, y);
+          bulk_commit_group();
+        }
+      }
+    };
     auto promote = [&](auto nc_tag, int y, int n_item, int g, bool store) {
       constexpr int NC = decltype(nc_tag)::value;
       const int col0 = (e >> 2) * NC;
@@ -422,22 +472,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool col_ok = n < N;
 #pragma unroll
       for (int j = 0; j < NC / 2; ++j) acc[j] = make_float2(0.f, 0.f);
-      const float* bs_row = Bs + (size_t(g) * (N / 128) + size_t(col_ok ? n / 128 : 0)) * kblocks;
+      // kr: K block within this pair's range [kb0, kb1) (the whole range
+      // unless K is split); bs_row starts at the range's first K block.
+      const float* bs_row = Bs + (size_t(g) * (N / 128) + size_t(col_ok ? n / 128 : 0)) * kblocks + kb0;
+      const int nkb = kb1 - kb0;
       float bs_win = 0.f;
-      for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        if ((kb & 31) == 0) bs_win = (col_ok && kb + lane < kblocks) ? __ldg(bs_row + kb + lane) : 0.f;
-        const float sb = __shfl_sync(0xffffffffu, bs_win, kb & 31);
+      for (int kr = 0; kr < nkb; ++kr, ++it) {
+        if ((kr & 31) == 0) bs_win = (col_ok && kr + lane < nkb) ? __ldg(bs_row + kr + lane) : 0.f;
+        const float sb = __shfl_sync(0xffffffffu, bs_win, kr & 31);
         const int j = gi % kAsStages;
         const int d = it % kAccBufs;
         const uint32_t dph = (it / kAccBufs) & 1u;
-        if (kb % kAsGroup == 0 &&
+        if (kr % kAsGroup == 0 &&
             !__all_sync(0xffffffffu, mbar_wait(&as_full[j], (gi / kAsStages) & 1u, abort_flag))) {
           raise_error(err, abort_flag, kSiteEpilogueFull);
           ok = false;
           return;
         }
-        const float sa = as_stage[(j * kAsGroup + kb % kAsGroup) * TM + row];
-        if (kb % kAsGroup == kAsGroup - 1 || kb == kblocks - 1) {
+        const float sa = as_stage[(j * kAsGroup + kr % kAsGroup) * TM + row];
+        if (kr % kAsGroup == kAsGroup - 1 || kr == nkb - 1) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&as_empty[j]);
           ++gi;
@@ -471,34 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (y < M && col_ok && store) {
-        // The warp's 32 x NC block leaves as 128-byte-wide boxes (64 bf16 or
-        // 32 float32 columns), at most kBoxesPerWarp at a time through the
-        // staging boxes; chunk c (16 bytes) of row r sits at 16-byte
-        // position c ^ (r & 7) of the row (128-byte swizzle).
-        constexpr int kBoxCols = F32 ? 32 : 64;
-        constexpr int kBoxes = NC / kBoxCols;
-        constexpr int kPer = kBoxes < kBoxesPerWarp ? kBoxes : kBoxesPerWarp;
-#pragma unroll
-        for (int r = 0; r < kBoxes / kPer; ++r) {
-          if (lane == 0) bulk_wait_group_read0();   // earlier stores have left the staging boxes
-          __syncwarp();
-#pragma unroll
-          for (int h = 0; h < kPer; ++h) {
-            uint8_t* dst = stg + h * kStageC + lane * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(dst + ((c ^ (lane & 7)) << 4)) = out_chunk<F32>(acc, r * kPer + h, c);
-          }
-          fence_async_shared();   // generic-proxy writes become visible to the TMA engine
-          __syncwarp();
-          if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < kPer; ++h) tma_store_2d(&tmC, stg + h * kStageC, n + (r * kPer + h) * kBoxCols, y);
-            bulk_commit_group();
-          }
-        }
-      }
+      if (y < M && col_ok && store) store_block(nc_tag, y, n);
     };
     for (int t = pair; ok; t += num_pairs) {
       const Items it_sh{items_sh[0], items_sh[1]};
@@ -515,21 +541,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      // Grouped: this CTA's rows are stored in the pass of their own group.
-      const bool store = row_group == nullptr || half_group(row_group, mt * 2 * TM + rank * TM, M) == g;
+      // Grouped: this CTA's rows are stored in the pass of their own group;
+      // split K: after the exchange below.
+      const bool store = ksplit == 1 && (row_group == nullptr || half_group(row_group, mt * 2 * TM + rank * TM, M) == g);
       const int y = mt * 2 * TM + rank * TM + quarter * 32;
       if (half < 0)
         promote(std::integral_constant<int, kCols>{}, y, nt * PN, g, store);
       else
         promote(std::integral_constant<int, kCols / 2>{}, y, nt * PN + half * HN, g, store);
     }
+    if (ksplit > 1) {
+      // Split K: exchange the column halves between the two pairs (the
+      // control warps take part in the cluster barrier at the end of their
+      // branch).  This CTA's stages are free: every MMA of its pair has
+      // completed, and every copy into them has been consumed.  (The cluster
+      // rank is read again here rather than kept live across the K loop.)
+      const int xrank = int(cluster_ctarank());   // ksplit == 2 here
+      const int xslice = xrank >> 1;
+      const bool keep = (e >> 2) == xslice;
+      constexpr int kXPitch = kCols + 4;   // floats per row, rows 16 bytes apart in bank terms
+      float* xbuf = reinterpret_cast<float*>(smem);   // [TM][kXPitch]: the half this pair gives away
+      if (!keep) {
+        float4* dst = reinterpret_cast<float4*>(xbuf + size_t(row) * kXPitch);
+#pragma unroll
+        for (int i = 0; i < kCols / 4; ++i)
+          dst[i] = make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
+      }
+      cluster_sync();
+      if (keep && ok && !*abort_flag) {
+        int mt, nt;
+        tile_coords(pair, m_tiles, n_tiles, mt, nt);   // split K: one whole tile per cluster
+        const uint32_t peer = map_shared_rank(smem_u32(xbuf + size_t(row) * kXPitch), uint32_t(xrank ^ 2));
+#pragma unroll
+        for (int c = 0; c < kCols / 16; ++c) {
+          float4 v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] = ld_shared_cluster_f4(peer + uint32_t((c * 16 + 4 * i) * 4));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float2& a0 = acc[c * 8 + 2 * i];
+            float2& a1 = acc[c * 8 + 2 * i + 1];
+            a0.x += v[i].x;
+            a0.y += v[i].y;
+            a1.x += v[i].z;
+            a1.y += v[i].w;
+          }
+        }
+        const int y = mt * 2 * TM + (xrank & 1) * TM + quarter * 32;
+        const int n = nt * PN + xslice * kCols;
+        if (y < M && n < N) store_block(std::integral_constant<int, kCols>{}, y, n);
+      }
+    }
     if (lane == 0) bulk_wait_group0();   // the staging buffer stays valid until the stores are done
   }
 
   __syncwarp();
+  if (ksplit > 1 && (threadIdx.x >> 5) < 4) cluster_sync();   // the exchange barrier of the promotion warps
   tc_fence_before();
   __syncthreads();
-  cluster_sync();   // neither CTA leaves while the other may still reach its shared memory
+  cluster_sync();   // no CTA leaves while another may still reach its shared memory
   // Re-read the TMEM address here instead of keeping it live across the role
   // branches, where the register budget is the smaller warpgroup's.
   if ((threadIdx.x >> 5) == 1) {
@@ -544,8 +614,8 @@ int w8a8_pair_tiles(int M, int N) { return ((M + 2 * TM - 1) / (2 * TM)) * ((N +
 
 namespace {
 
-template <bool F32>
-cudaError_t launch_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+template <bool F32, int ksplit>
+cudaError_t launch_pair_k(const GemmW8A8Args& p, int pairs, cudaStream_t stream) {
   static bool attr_done[64] = {};
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
@@ -554,35 +624,43 @@ cudaError_t launch_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream
     // The setmaxnreg split assumes the launch register count; refuse to run
     // any build where it differs.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, w8a8_pair_kernel<F32>);
+    e = cudaFuncGetAttributes(&fa, w8a8_pair_kernel<F32, ksplit>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(w8a8_pair_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    e = cudaFuncSetAttribute(w8a8_pair_kernel<F32, ksplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_done[device] = true;
   }
-  const int tiles = w8a8_pair_tiles(p.M, p.N);
-  const int max_pairs = dev.num_sms / 2;
-  // Dense problems whose tiles fit on half of the pairs run every tile as two
-  // 256 x 128 halves, one pair each (see make_items).
-  const int items = (p.row_group == nullptr && 2 * tiles <= max_pairs) ? 2 * tiles : tiles;
-  const int pairs = items < max_pairs ? items : max_pairs;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(2 * pairs), 1, 1);
+  cfg.gridDim = dim3(unsigned(2 * ksplit * pairs), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = unsigned(2 * ksplit);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel<F32>, p.tmA, p.tmB, p.tmAsG, p.tmC, p.Bs, p.row_group, p.groups, p.M,
-                            p.N, p.K, p.err);
+  return cudaLaunchKernelEx(&cfg, w8a8_pair_kernel<F32, ksplit>, p.tmA, p.tmB, p.tmAsG, p.tmC, p.Bs, p.row_group,
+                            p.groups, p.M, p.N, p.K, p.err);
+}
+
+template <bool F32>
+cudaError_t launch_pair(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStream_t stream) {
+  const int tiles = w8a8_pair_tiles(p.M, p.N);
+  const int max_pairs = dev.num_sms / 2;
+  // Dense problems whose tiles fit on half of the pairs run each tile on two
+  // pairs: split over K when the K range is long (kSplitMinKBlocks blocks or
+  // more), otherwise as two 256 x 128 halves (see make_items).
+  const bool two_per_tile = p.row_group == nullptr && 2 * tiles <= max_pairs;
+  if (two_per_tile && p.K / BK >= kSplitMinKBlocks) return launch_pair_k<F32, 2>(p, tiles, stream);
+  const int items = two_per_tile ? 2 * tiles : tiles;
+  return launch_pair_k<F32, 1>(p, items < max_pairs ? items : max_pairs, stream);
 }
 
 }  // namespace

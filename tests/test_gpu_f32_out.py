@@ -48,6 +48,7 @@ def _check_pair(c16, c32, ref, what):
     (1000, 2432, 1024),    # CTA-pair kernel, half-width last column tile
     (2200, 4992, 512),     # CTA-pair kernel, last-round tiles split in 256 x 128 halves
     (256, 7168, 256),      # CTA-pair kernel, every tile as two 256 x 128 halves
+    (256, 4992, 12288),    # CTA-pair kernel, K split over two pairs per tile
 ])
 def test_w8a8_f32_out(lib, M, N, K):
     x = synth.activations(M + K, M, K)

@@ -55,6 +55,8 @@ def gpu_w8a8(a, As, b, Bs, ldc_pad=0, lds_pad=0):
     (256, 7168, 512),      # CTA-pair path, 28 tiles all run as 56 half tiles (too many 128 x 128 tiles to split K)
     (200, 6144, 384),      # all halves, ragged second CTA of every pair
     (130, 4992, 256),      # all halves, the last tile's second half lies wholly past N
+    (200, 4992, 12416),    # CTA-pair path with K split over two pairs per tile: ragged M, a half-width
+                           # last column tile, 97 K blocks split 48 / 49
 ])
 def test_w8a8_matches_oracle(lib, M, N, K):
     a, As, b, Bs = w8a8_inputs(M + N + K, M, N, K)
