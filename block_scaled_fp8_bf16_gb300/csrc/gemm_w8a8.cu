@@ -12,11 +12,12 @@
 //   warp 0      TMA producer: A tile [128 x 128 B], B tile [128 x 128 B] and
 //               the tile rows' activation scales As[kb, m0..m0+127] per 128-K
 //               block into a 6-stage shared-memory ring.
-//   warp 1      allocates all 512 TMEM columns; one thread issues four
-//               tcgen05.mma kind::f8f6f4 (K = 32 each) per K block into one
-//               of four 128-column partial buffers, so the tensor cores run up
-//               to three K blocks ahead of the promotion.
-//   warps 2..9  promotion + epilogue: each thread owns one row and 64
+//   warp 1      allocates all 512 TMEM columns.
+//   warps 1, 2  MMA issuers (one in the fused form): one thread each issues
+//               the four tcgen05.mma kind::f8f6f4 (K = 32 each) of alternate
+//               K blocks into one of four 128-column partial buffers, so the
+//               tensor cores run up to three K blocks ahead of the promotion.
+//   next 8      promotion + epilogue: each thread owns one row and 64
 //               columns of the 128x128 tile; per K block it reads its partial
 //               with tcgen05.ld, releases the buffer, and does
 //               acc = fma(partial, As[kb, m] * Bs[n/128, kb], acc).
