@@ -50,6 +50,8 @@
 // (gemm_w8a8_pair.cu).
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -224,7 +226,6 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
   const int quarter = warp & 3;
   const int half = (warp - Q::kCtlWarps) >> 2;
   const int row_in_tile = quarter * 32 + lane;
-  int last_mt = 0, last_nt = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -383,8 +384,6 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
         if (g >= G && threadIdx.x == 32 * Q::kCtlWarps) atomicCAS(err, 0, kDevErrW8A8 | kSiteBadGroup);
         continue;
       }
-      last_mt = mt;
-      last_nt = nt;
       const int m = mt * BM + row_in_tile;
       const bool row_ok = m < M;
 #pragma unroll
@@ -577,34 +576,63 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
 
   __syncwarp();   // single-lane roles rejoin their warp before the aligned barriers below
   if (split > 1) {
-    // One tile per cluster: sum the ranks' accumulators through distributed
-    // shared memory, in rank order, into rank 0.  Every thread of every CTA
-    // reaches both cluster barriers, also after an abort.
+    // One tile per cluster: every rank writes the valid rows (m < M) of its
+    // accumulator tile to its shared memory; after a cluster barrier each
+    // rank sums its share of those rows (split evenly) over all ranks' tiles
+    // through distributed shared memory, in rank order (so the result is the
+    // rank-0-first sum), and stores them.
+    // All of a CTA's threads take part, consecutive threads on consecutive
+    // rows of one 4-column group (contiguous 16-byte reads).  Every thread of
+    // every CTA reaches both cluster barriers, also after an abort.
     const bool epi = warp >= Q::kCtlWarps && warp < Q::kCtlWarps + kEpiWarps;
-    const int m = last_mt * BM + row_in_tile;
-    const bool row_ok = epi && m < M;
     float4* red = reinterpret_cast<float4*>(smem);   // [BN/4][BM] float4, reuses stages 0-1
-    if (row_ok && rank != 0) {
+    // Split K runs one tile per cluster: every thread can name it.
+    int tile_mt, tile_nt;
+    tile_coords(cluster_id, m_tiles, n_tiles, tile_mt, tile_nt);
+    const int valid = min(BM, M - tile_mt * BM);   // rows of the tile below M
+    if (epi && row_in_tile < valid) {
 #pragma unroll
       for (int j4 = 0; j4 < kColsPerThread / 4; ++j4)
         red[(half * (kColsPerThread / 4) + j4) * BM + row_in_tile] =
             make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
     }
     cluster_sync();
-    if (row_ok && rank == 0) {
-      for (int r = 1; r < split; ++r) {
-        const uint32_t base = map_shared_rank(smem_u32(red), uint32_t(r));
+    if (!*abort_flag) {
+      const int per = (valid + split - 1) / split;
+      const int r0 = min(valid, rank * per);
+      const int rows = min(valid, r0 + per) - r0;    // rows this rank sums
+      const int items = rows * (BN / 4);             // float4 items of those rows
+      uint32_t peer[kMaxSplitK];
 #pragma unroll
-        for (int j4 = 0; j4 < kColsPerThread / 4; ++j4) {
-          const float4 v =
-              ld_shared_cluster_f4(base + uint32_t(((half * (kColsPerThread / 4) + j4) * BM + row_in_tile) * 16));
-          acc[4 * j4] += v.x;
-          acc[4 * j4 + 1] += v.y;
-          acc[4 * j4 + 2] += v.z;
-          acc[4 * j4 + 3] += v.w;
+      for (int p = 0; p < kMaxSplitK; ++p) peer[p] = map_shared_rank(smem_u32(red), uint32_t(p < split ? p : 0));
+      for (int idx = int(threadIdx.x); idx < items; idx += int(blockDim.x)) {
+        const int r = r0 + idx % rows;               // row within the tile
+        const int c4 = idx / rows;                   // 4-column group
+        const int m = tile_mt * BM + r;
+        const uint32_t off = uint32_t((c4 * BM + r) * 16);
+        float4 v[kMaxSplitK];
+#pragma unroll
+        for (int p = 0; p < kMaxSplitK; ++p)
+          if (p < split) v[p] = ld_shared_cluster_f4(peer[p] + off);
+        float4 sum = v[0];
+#pragma unroll
+        for (int p = 1; p < kMaxSplitK; ++p) {
+          if (p < split) {
+            sum.x += v[p].x;
+            sum.y += v[p].y;
+            sum.z += v[p].z;
+            sum.w += v[p].w;
+          }
+        }
+        {
+          OutT* dst = C + size_t(m) * ldc + size_t(tile_nt) * BN + size_t(4 * c4);
+          if constexpr (std::is_same<OutT, float>::value) {
+            *reinterpret_cast<float4*>(dst) = sum;
+          } else {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
+          }
         }
       }
-      if (!*abort_flag) store_row64(C + size_t(m) * ldc + size_t(last_nt) * BN + half * kColsPerThread, acc);
     }
     cluster_sync();
   }
