@@ -663,8 +663,9 @@ cudaError_t launch_single(const GemmW8A8Args& p, const DeviceInfo& dev, cudaStre
   const int tiles = m_tiles * n_tiles;
   const int kblocks = p.K / BK;
   // K is split over at most 4 CTAs: with 16 tiles of K = 7168 at M = 16 or
-  // 128, 8-way splits took 19 and 33 us against 12.4 and 16 us for 4-way
-  // (the 8-rank reduction costs more than the K blocks it saves).
+  // 128, 8-way splits took 17.6 and 19.8 us against 12.4 and 13.9 us for
+  // 4-way, also with the reduce-scatter (eight-CTA clusters of full-SM CTAs
+  // are the cost, not the sum).
   constexpr int kSplitCap = 4;
   int split = 1;
   if (tiles * 2 <= dev.num_sms && p.row_group == nullptr) {
