@@ -220,7 +220,7 @@ fp8blk_status run_w8a16(const void* x, int64_t ldx, const void* b, int64_t ldb, 
   p.out_f32 = f32;
   p.err = dev.err_word;
   const bool decode = M <= kW8A16DecodeMaxM;
-  const int tile_m = decode ? (M <= 16 ? 16 : 32) : w8a16_pick_tile_m(M);
+  const int tile_m = decode ? (M <= 16 ? 16 : 32) : w8a16_pick_tile_m(M, N, fmt, dev.num_sms);
   st = make_map(p.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, uint64_t(K), uint64_t(N), uint64_t(ldb), 128, 128);
   if (st != FP8BLK_OK) return st;
   st = make_map(p.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, uint64_t(K), uint64_t(M), uint64_t(ldx) * 2, 64,

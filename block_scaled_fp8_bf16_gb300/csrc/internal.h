@@ -150,14 +150,14 @@ struct GemmW8A16Args {
   void* C;
   int64_t ldc;
   int M, N, K;
-  int tile_m;         // token tile (MMA N): 16, 32, 64 or 128
+  int tile_m;         // token tile (MMA N): 16, 32, 64, 128 or 256 (UE8M0 only)
   bool pdl;           // launch with programmatic stream serialisation
   bool out_f32;       // C is float32 (ldc in float32 elements), else bf16
   int* err;
 };
 constexpr int kW8A16TileN = 128;
-constexpr int kW8A16MaxTileM = 128;
-int w8a16_pick_tile_m(int64_t M);
+constexpr int kW8A16MaxTileM = 256;
+int w8a16_pick_tile_m(int64_t M, int64_t N, int fmt, int num_sms);
 cudaError_t launch_gemm_w8a16(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t s);
 
 // Decode-size W8A16 (M <= tile_m, tile_m 16 or 32).

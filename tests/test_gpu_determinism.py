@@ -74,6 +74,7 @@ def test_w8a8_ue8m0_deterministic(lib, M, N, K):
     (1024, 2048, 2048),    # 128-token tiles, two issuers (taking turns for UE8M0)
     (64, 2048, 4096),      # 64-token tiles
     (128, 2048, 7168),     # K split over a cluster
+    (1024, 7168, 1024),    # 256-token tiles for UE8M0, two issuers taking turns
 ])
 def test_w8a16_deterministic(lib, M, N, K, fmt):
     x = tg.activations(M + N, M, K)

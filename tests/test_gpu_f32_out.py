@@ -70,6 +70,7 @@ def test_w8a8_f32_out(lib, M, N, K):
     (5, 4096, 4096, 0),    # decode-size kernel, K split over a cluster
     (100, 256, 512, 0),    # token-tiled kernel
     (200, 384, 512, 1),
+    (612, 4864, 384, 1),   # token-tiled kernel, 256-token tiles
 ])
 def test_w8a16_f32_out(lib, M, N, K, fmt):
     x = synth.activations(M * 3 + K, M, K, outliers=True)

@@ -186,6 +186,31 @@ def test_gemm_w8a16(lib, M, N, K, fmt):
     assert_gemm_close(out, ref, f"w8a16 fmt{fmt} {M}x{N}x{K}")
 
 
+# 256-token tiles (UE8M0 only; on 152 SMs taken when they need fewer rounds
+# than 128-token tiles, a 256-token tile counted as 1.41): whole tiles, a
+# ragged last tile whose last two 64-token epilogue slices lie wholly past M,
+# an odd K block count (the two MMA issuers swap parity every tile), and more
+# tiles than SMs (the one accumulator reused within a CTA).
+@pytest.mark.parametrize("M,N,K", [(768, 6528, 256), (612, 4864, 384), (1100, 6528, 128)])
+def test_gemm_w8a16_ue8m0_tile256(lib, M, N, K):
+    x = synth.activations(M + N + K, M, K, outliers=True)
+    b, sc = synth.ue8m0_weights(N + K, N, K)
+    out = gpu_w8a16(x, b, sc, 1)
+    assert_gemm_close(out, O.gemm_w8a16_ue8m0(x, b, sc), f"w8a16 ue8m0 tile256 {M}x{N}x{K}")
+
+
+def test_w8a16_tile256_one_hot_rows_exact(lib):
+    """Token r holds a single 1.0 at column r mod K: C row r is then exactly
+    the decoded weight column times its block scale, so every token lands in
+    its own output row through the 256-token tile's streamed epilogue."""
+    M, N, K = 530, 19456, 256
+    x = np.zeros((M, K), dtype=np.uint16)
+    x[np.arange(M), np.arange(M) % K] = 0x3F80
+    b, e = synth.ue8m0_weights(3, N, K)
+    out = gpu_w8a16(x, b, e, 1)
+    assert np.array_equal(out, O.gemm_w8a16_ue8m0(x, b, e))
+
+
 def test_w8a16_ue8m0_full_size_sampled(lib):
     M, N, K = 4096, 7168, 2048
     x = synth.activations(1, M, K)
