@@ -88,8 +88,8 @@ struct Cfg {
   static constexpr int kStages = TM == 16 ? 8 : (TM == 32 ? 7 : (TM == 64 ? 5 : (TM == 128 ? 4 : 2)));
   static constexpr size_t kXOffset = size_t(kStages) * kStageBytes;   // activation ring (split ring)
   static constexpr size_t kRingBytes = kXOffset + (kSplitRing ? size_t(kXStages) * kXHalf : 0);
-  // TM = 256: a 32 x 32 bf16 transpose buffer per epilogue warp.
-  static constexpr size_t kOutStage = kSplitRing ? size_t(kEpiWarps) * 32 * 32 * 2 : 0;
+  // A 32 x 32 bf16 transpose buffer per epilogue warp (bf16 output).
+  static constexpr size_t kOutStage = size_t(kEpiWarps) * 32 * 32 * 2;
   // FP32 partial buffers: as many as fit next to the A blocks (the promotion
   // round trip per K block is long compared with a narrow tile's MMA time).
   // TM = 256 (UE8M0 only) has one accumulator: the tensor pipe waits while
@@ -132,6 +132,25 @@ __device__ __forceinline__ void store_col(OutT* __restrict__ C, int64_t ldc, int
   for (int j = 0; j < COLS; ++j) {
     if (m0 + j < M) C[size_t(m0 + j) * ldc + n] = to_out(acc[j], C);
   }
+}
+
+// Stores 32 tokens of C for the warp's 32 weight rows: lane l holds v[j] =
+// C[m0 + j][n0 + l].  The values go through the warp's 32 x 32 transpose
+// buffer in shared memory, so C is written in 16-byte pieces of its rows
+// (eight tokens per pass, four lanes per token) instead of one 2-byte store
+// per lane and token.
+__device__ __forceinline__ void store_rows32_bf16(__nv_bfloat16* __restrict__ C, int64_t ldc, int M, int m0, int n0,
+                                                  const float* v, __nv_bfloat16* tr, int lane) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) tr[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int r = q * 8 + (lane >> 2);
+    const uint4 val = *reinterpret_cast<const uint4*>(tr + r * 32 + (lane & 3) * 8);
+    if (m0 + r < M) *reinterpret_cast<uint4*>(C + size_t(m0 + r) * ldc + n0 + (lane & 3) * 8) = val;
+  }
+  __syncwarp();
 }
 
 // OutT: __nv_bfloat16 (rounded to nearest even) or float (the accumulator as is).
@@ -456,13 +475,11 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
     // ------------------------------------------------------------ epilogue, UE8M0
     // The whole K range is in the one accumulator; this warp's 64 token
     // columns are read 32 at a time and the buffer is released after the last
-    // read.  bf16 output goes through a per-warp transpose in shared memory
-    // (thread = weight row while reading, 16-byte pieces of C rows while
-    // storing): a 2-byte store per thread and token took most of the time.
+    // read.  bf16 output goes through the warp's transpose buffer (a 2-byte
+    // store per thread and token took most of the time).
     griddep_wait();   // the output may still be read or written by the previous kernel
     __nv_bfloat16* tr = reinterpret_cast<__nv_bfloat16*>(smem + Q::kRingBytes) +
                         (warp - kCtlWarps - Q::kDecWarps) * (32 * 32);
-    (void)tr;
     uint32_t i = 0;
     for (int t = cluster_id; t < num_tiles; t += num_clusters, ++i) {
       int nt, mt;
@@ -486,30 +503,20 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
           __syncwarp();
           if (lane == 0) mbar_arrive(&dempty[0]);
         }
-        if constexpr (sizeof(OutT) == 2) {
+        float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) tr[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(p[j]));
-          __syncwarp();
-          // eight tokens per pass, four lanes per token, eight weight rows per lane
-          const int n0 = nt * BN + quarter * 32 + (lane & 3) * 8;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = q * 8 + (lane >> 2);
-            const uint4 val = *reinterpret_cast<const uint4*>(tr + r * 32 + (lane & 3) * 8);
-            if (m0 + c * 32 + r < M) *reinterpret_cast<uint4*>(C + size_t(m0 + c * 32 + r) * ldc + n0) = val;
-          }
-          __syncwarp();
-        } else {
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
+        if constexpr (sizeof(OutT) == 2)
+          store_rows32_bf16(C, ldc, M, m0 + c * 32, nt * BN + quarter * 32, v, tr, lane);
+        else
           store_col<32>(C, ldc, M, m0 + c * 32, n, v);
-        }
       }
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue
     griddep_wait();   // the output may still be read or written by the previous kernel
+    __nv_bfloat16* tr = reinterpret_cast<__nv_bfloat16*>(smem + Q::kRingBytes) +
+                        (warp - kCtlWarps - Q::kDecWarps) * (32 * 32);
     uint32_t acc_it = 0;
     bool ok = true;
     const float* bs32 = static_cast<const float*>(scales);
@@ -546,7 +553,15 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
         __syncwarp();
         if (lane == 0) mbar_arrive(&dempty[d]);
       }
-      if (ok && split == 1) store_col<EC>(C, ldc, M, mt * TM + col0, nt * BN + row, acc);
+      if (ok && split == 1) {
+        if constexpr (sizeof(OutT) == 2) {
+#pragma unroll
+          for (int c = 0; c < EC / 32; ++c)
+            store_rows32_bf16(C, ldc, M, mt * TM + col0 + c * 32, nt * BN + quarter * 32, acc + c * 32, tr, lane);
+        } else {
+          store_col<EC>(C, ldc, M, mt * TM + col0, nt * BN + row, acc);
+        }
+      }
     }
   }
 
