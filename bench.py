@@ -424,6 +424,40 @@ def reference_arm(args, world, rank):
     }
 
 
+def graph_time(calls, reps=10):
+    """Median time per call (us) of `calls` captured once in a CUDA graph and
+    replayed `reps` times (three untimed replays first); raises if a kernel
+    set the library's device error word."""
+    import torch
+
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for c in calls:
+            c()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / len(calls))
+    if fp8blk.fp8blk_device_error() != 0:
+        raise RuntimeError("device error word set")
+    return statistics.median(times) * 1e3     # us per call
+
+
 # ---------------------------------------------------------------- sweep
 
 def sweep(out_path, kinds=None):
@@ -437,33 +471,6 @@ def sweep(out_path, kinds=None):
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     pk = peaks()
     rows = []
-
-    def graph_time(calls, reps=10):
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            for c in calls:
-                c()
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for c in calls:
-                c()
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            g.replay()
-            e1.record()
-            torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1) / len(calls))
-        if fp8blk.fp8blk_device_error() != 0:
-            raise RuntimeError("device error word set")
-        return statistics.median(times) * 1e3     # us per call
 
     def record(kind, M, N, K, us, flop, bytes_, tensor_peak):
         t_tensor = flop / (tensor_peak * 1e12)
@@ -680,9 +687,10 @@ def run_case(spec: str, iters: int):
 # ---------------------------------------------------------------- probe
 
 def probe():
-    """Memory-system figures that frame the rooflines (no kernel of this
-    repository runs): device read, write and copy rates by size with torch
-    reductions, fills and copies, and the host link's copy-engine rates for
+    """Memory-system figures that frame the rooflines: device read, write and
+    copy rates by size with torch reductions, fills and copies, the library's
+    plain streaming-read kernel on the weight-set sizes of the decode-size
+    workloads, and the host link's copy-engine rates for
     one 33.5 MB transfer (the headline step's activations or output), alone
     and with both directions at once.  One JSON line per measurement."""
     import torch
@@ -709,6 +717,21 @@ def probe():
             t = best(fn)
             print(json.dumps({"probe": "hbm", "op": what, "mib": nbytes >> 20, "gb_s": round(moved / t / 1e9, 1)}))
         del a, b
+    # The library's plain streaming-read kernel on the decode-size weight-set
+    # sizes, in CUDA-graph replays over rotated copies larger than 2x L2 (as
+    # the sweep times the GEMMs): the rate that any kernel reading a weight
+    # set of that size once can reach.
+    import block_scaled_fp8_bf16_gb300 as fp8blk
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    for what, nbytes in (("2048x7168 codes", 2048 * 7168), ("4096x4096 codes", 4096 * 4096),
+                         ("4096x14336 codes", 4096 * 14336), ("28672x4096 codes", 28672 * 4096),
+                         ("512 MiB", 1 << 29)):
+        reps = max(2, -(-(1 << 28) // nbytes))
+        bufs = [torch.full((nbytes,), i, dtype=torch.uint8, device=dev) for i in range(reps)]
+        us = graph_time([lambda b=b: fp8blk.fp8blk_debug_stream_read(b, sink) for b in bufs])
+        print(json.dumps({"probe": "hbm, plain read kernel (fp8blk_debug_stream_read), CUDA graph", "op": what,
+                          "mb": round(nbytes / 1e6, 1), "us": round(us, 2), "gb_s": round(nbytes / us / 1e3, 1)}))
+        del bufs
     # Per-kernel floor: a one-element kernel replayed 200 times in a CUDA graph.
     t1 = torch.zeros(1, device=dev)
     g = torch.cuda.CUDAGraph()

@@ -61,6 +61,7 @@ EXPORTS = {
     "fp8blk_validate_weights": (_I32, [_P, _I64, _P, _I32, _I64, _I64, _P, _P]),
     "fp8blk_debug_decode_e4m3": (_I32, [_P, _I64, _I32, _P, _P]),
     "fp8blk_debug_group_scale": (_I32, [_P, _I64, _P, _P, _P, _P]),
+    "fp8blk_debug_stream_read": (_I32, [_P, _I64, _P, _P]),
     "fp8blk_debug_wait_timeout": (_I32, [_I64, _P]),
     "fp8blk_query_constraints": (_I32, [_P]),
     "fp8blk_status_string": (ctypes.c_char_p, [_I32]),
@@ -297,6 +298,15 @@ def fp8blk_debug_decode_e4m3(codes, exp_shift, out, stream=None):
 
 
 DIAG_TIMEOUT_CODE = 0x4F01   # FP8BLK_DIAG_TIMEOUT_CODE in the header
+
+
+def fp8blk_debug_stream_read(buf, sink, stream=None):
+    """Reads every byte of the contiguous device tensor buf with the plain
+    streaming-read kernel and XORs its 32-bit words into sink (a one-element
+    int32/uint32 device tensor)."""
+    assert buf.is_contiguous(), "fp8blk_debug_stream_read reads a contiguous buffer"
+    _check(_L().fp8blk_debug_stream_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink), _stream(stream)),
+           "fp8blk_debug_stream_read")
 
 
 def fp8blk_debug_wait_timeout(limit_ns: int, stream=None):

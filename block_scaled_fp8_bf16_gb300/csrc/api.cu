@@ -564,6 +564,17 @@ fp8blk_status fp8blk_debug_group_scale(const float* amax, int64_t n, float* s_ou
       launch_debug_group_scale(amax, n, s_out, divisor_out, recip_out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8blk_status fp8blk_debug_stream_read(const void* p, int64_t bytes, uint32_t* sink, fp8blk_stream_t stream) {
+  if (bytes < 0 || bytes % 16 != 0) return FP8BLK_ERR_INVALID_ARG;
+  if (bytes == 0) return FP8BLK_OK;
+  if (!p || !sink) return FP8BLK_ERR_INVALID_ARG;
+  if (!aligned16(p) || (reinterpret_cast<uintptr_t>(sink) & 3u) != 0) return FP8BLK_ERR_MISALIGNED;
+  DeviceInfo dev;
+  fp8blk_status st = device_info(dev);
+  if (st != FP8BLK_OK) return st;
+  return cuda_status(launch_debug_stream_read(p, bytes / 16, sink, dev.num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 fp8blk_status fp8blk_debug_wait_timeout(int64_t limit_ns, fp8blk_stream_t stream) {
   if (limit_ns < 1000 || limit_ns > 100000000) return FP8BLK_ERR_INVALID_ARG;
   DeviceInfo dev;

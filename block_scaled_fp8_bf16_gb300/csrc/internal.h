@@ -78,6 +78,7 @@ cudaError_t launch_validate(const ValidateArgs& p, const DeviceInfo& dev, cudaSt
 cudaError_t launch_debug_decode(const void* codes, int64_t n, int exp_shift, void* out, cudaStream_t s);
 cudaError_t launch_debug_group_scale(const float* amax, int64_t n, float* s, float* ds, float* y, cudaStream_t st);
 cudaError_t launch_debug_wait_timeout(int64_t limit_ns, int code, int* err, cudaStream_t s);
+cudaError_t launch_debug_stream_read(const void* p, int64_t words16, uint32_t* sink, int num_sms, cudaStream_t s);
 
 // ------------------------------------------------------------------ W8A8
 struct GemmW8A8Args {

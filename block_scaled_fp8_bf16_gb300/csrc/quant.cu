@@ -372,6 +372,44 @@ cudaError_t launch_debug_wait_timeout(int64_t limit_ns, int code, int* err, cuda
   return cudaGetLastError();
 }
 
+// A plain read-only stream: n 16-byte words, eight loads in flight per
+// thread (grid-stride), every 32-bit word XORed into *sink (one atomic per
+// CTA), so that nothing of the stream can be dropped.
+constexpr int kReadThreads = 512;
+__global__ void __launch_bounds__(kReadThreads) debug_stream_read_kernel(const uint4* __restrict__ p, int64_t n,
+                                                                          uint32_t* __restrict__ sink) {
+  constexpr int U = 8;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  uint32_t acc = 0;
+  for (; i + (U - 1) * stride < n; i += U * stride) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = __ldcs(p + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+  for (; i < n; i += stride) {
+    const uint4 v = __ldcs(p + i);
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+  __shared__ uint32_t warp_x[kReadThreads / 32];
+  if ((threadIdx.x & 31) == 0) warp_x[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+    for (int w = 0; w < kReadThreads / 32; ++w) b ^= warp_x[w];
+    atomicXor(sink, b);
+  }
+}
+
+cudaError_t launch_debug_stream_read(const void* p, int64_t words16, uint32_t* sink, int num_sms, cudaStream_t s) {
+  debug_stream_read_kernel<<<4 * num_sms, kReadThreads, 0, s>>>(static_cast<const uint4*>(p), words16, sink);
+  return cudaGetLastError();
+}
+
 // Runs the quantisers' scale arithmetic on n group maxima: s = group_scale,
 // and the divisor make_divisor(s) forms (scaled divisor and its reciprocal).
 __global__ void debug_group_scale_kernel(const float* __restrict__ amax, int64_t n, float* __restrict__ s_out,

@@ -401,6 +401,20 @@ FP8BLK_API fp8blk_status fp8blk_debug_group_scale(const float* amax, int64_t n, 
                                        fp8blk_stream_t stream);
 
 /*
+ * Diagnostic: the device's rate for a plain read-only stream, the bound on
+ * what any kernel that reads a weight set once can reach (no counterpart in
+ * the pages; it frames the decode-size rooflines).  Reads `bytes` bytes at p
+ * with 16-byte loads (eight in flight per thread, a grid-stride loop over
+ * four 512-thread CTAs per SM, streaming cache hint) and XORs every 32-bit
+ * word into *sink (*sink ^= w0 ^ w1 ^ ...; the caller sets its initial
+ * value).  p: device, 16-byte aligned; bytes % 16 == 0 (else
+ * FP8BLK_ERR_MISALIGNED / FP8BLK_ERR_INVALID_ARG before any device work);
+ * sink: device uint32, 4-byte aligned.  Asynchronous on stream.
+ */
+FP8BLK_API fp8blk_status fp8blk_debug_stream_read(const void* p, int64_t bytes, uint32_t* sink,
+                                       fp8blk_stream_t stream);
+
+/*
  * Failure-detection check of the bounded waits (no counterpart in the pages;
  * it exercises the library's own error path).  Launches one warp that
  * initialises an mbarrier nobody arrives on and waits for it with the same

@@ -179,6 +179,18 @@ def test_wait_timeout_diag_argument_errors(fp8blk):
         assert L.fp8blk_debug_wait_timeout(bad, None) == 1   # FP8BLK_ERR_INVALID_ARG, no device work
 
 
+def test_stream_read_diag_argument_errors(fp8blk):
+    L = fp8blk._L()
+    r = lambda p=P, n=4096, sink=P: L.fp8blk_debug_stream_read(p, n, sink, None)
+    assert r(n=-16) == 1
+    assert r(n=100) == 1        # not a multiple of 16 bytes
+    assert r(n=0) == 0
+    assert r(p=None) == 1
+    assert r(sink=None) == 1
+    assert r(p=MIS) == 3
+    assert r(sink=P + 2) == 3
+
+
 def test_grouped_argument_errors(fp8blk):
     L = fp8blk._L()
     P = ctypes.c_void_p(16 * 1024)   # a fake, 16-byte aligned device address: never dereferenced on these paths
