@@ -75,6 +75,7 @@ def test_w8a8_ue8m0_deterministic(lib, M, N, K):
     (64, 2048, 4096),      # 64-token tiles
     (128, 2048, 7168),     # K split over a cluster
     (1024, 7168, 1024),    # 256-token tiles for UE8M0, two issuers taking turns
+    (4096, 7168, 2048),    # 256-token tiles over six rounds of the SMs (a release race showed in the last rounds)
 ])
 def test_w8a16_deterministic(lib, M, N, K, fmt):
     x = tg.activations(M + N, M, K)
