@@ -60,7 +60,9 @@ constexpr int kGroupN = 8;
 constexpr int kBarrierBytes = 512;
 constexpr int kCtlWarps = 3;      // producer, two MMA issuers; the decode warps follow
 
-template <int TM>
+// F32: float output (the 256-token tile then keeps eight decode warps: with
+// four, its float epilogue does not fit in the registers left).
+template <int TM, bool F32 = false>
 struct Cfg {
   // Epilogue warps: 4 (one per TMEM lane quarter), or 8 / 16 for the 128- /
   // 256-token tiles, where two / four warps share a lane quarter and split
@@ -68,10 +70,11 @@ struct Cfg {
   static constexpr int kEpiWarps = TM == 256 ? 16 : (TM == 128 ? 8 : 4);
   static constexpr int kEpiCols = TM / (kEpiWarps / 4);
   // Decode warps: two per TMEM lane quarter (each decodes half of the K
-  // block), except at TM = 64, where one per quarter keeps up with the
-  // narrower MMAs (at TM = 128 with two MMA issuers, eight decode warps
-  // measured 3-4 % faster than four).
-  static constexpr int kDecWarps = TM == 64 ? 4 : 8;
+  // block), except at TM = 64 and 256, where one per quarter keeps up with
+  // the MMAs (at TM = 128 with two MMA issuers, eight decode warps measured
+  // 3-4 % faster than four; at TM = 256 a decoded block feeds twice the MMA
+  // work, and four warps leave registers for the epilogue).
+  static constexpr int kDecWarps = (TM == 64 || (TM == 256 && !F32)) ? 4 : 8;
   static constexpr int kDecChunks = 8 / (kDecWarps / 4);   // 16-byte chunks of a row per decode warp
   static constexpr int kThreads = 32 * kCtlWarps + (kDecWarps + kEpiWarps) * 32;
   static constexpr int kStageX = TM * BK * 2;                  // bf16 activation tile
@@ -155,11 +158,11 @@ __device__ __forceinline__ void store_rows32_bf16(__nv_bfloat16* __restrict__ C,
 
 // OutT: __nv_bfloat16 (rounded to nearest even) or float (the accumulator as is).
 template <int TM, class OutT>
-__global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
+__global__ void __launch_bounds__(Cfg<TM, sizeof(OutT) == 4>::kThreads, Cfg<TM, sizeof(OutT) == 4>::kMinBlocks)
     w8a16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const void* __restrict__ scales, int fmt, OutT* __restrict__ C, int64_t ldc, int M,
                  int N, int K, int split, int* __restrict__ err) {
-  using Q = Cfg<TM>;
+  using Q = Cfg<TM, sizeof(OutT) == 4>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -473,10 +476,15 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
     }
   } else if constexpr (TM == 256) {
     // ------------------------------------------------------------ epilogue, UE8M0
-    // The whole K range is in the one accumulator; this warp's 64 token
-    // columns are read 32 at a time and the buffer is released after the last
-    // read.  bf16 output goes through the warp's transpose buffer (a 2-byte
-    // store per thread and token took most of the time).
+    // The whole K range is in the one accumulator, and the tensor pipe waits
+    // while it drains.  With bf16 output this warp reads all of its 64 token
+    // columns at once, stores them through its transpose buffer (a 2-byte
+    // store per thread and token took most of the time) and then releases the
+    // buffer.  (Releasing it between the reads and the stores, so that the
+    // next tile's MMAs overlap the stores, measured up to 8 % faster but gave
+    // wrong tiles in the last rounds of some runs on one GPU, a race whose
+    // cause is not found.)  Float output (64 more registers would spill) is
+    // read and stored 32 columns at a time.
     griddep_wait();   // the output may still be read or written by the previous kernel
     __nv_bfloat16* tr = reinterpret_cast<__nv_bfloat16*>(smem + Q::kRingBytes) +
                         (warp - kCtlWarps - Q::kDecWarps) * (32 * 32);
@@ -493,24 +501,35 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
       const uint32_t taddr = tmem_d + (uint32_t(quarter * 32) << 16) + uint32_t(col0);
       const int m0 = mt * TM + col0;
       const int n = nt * BN + row;
-#pragma unroll 1
-      for (int c = 0; c < EC / 32; ++c) {
-        uint32_t p[32];
-        tmem_ld_x32(taddr + uint32_t(c * 32), p);
+      static_assert(EC == 64, "two 32-column chunks per epilogue warp");
+      if constexpr (sizeof(OutT) == 2) {
+        uint32_t p[64];
+        tmem_ld_x32(taddr, p);
+        tmem_ld_x32(taddr + 32u, p + 32);
         tmem_ld_wait();
-        if (c == EC / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&dempty[0]);
-        }
-        float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
-        if constexpr (sizeof(OutT) == 2)
+        for (int c = 0; c < 2; ++c) {
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[c * 32 + j]);
           store_rows32_bf16(C, ldc, M, m0 + c * 32, nt * BN + quarter * 32, v, tr, lane);
-        else
+        }
+      } else {
+        (void)tr;
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          uint32_t p[32];
+          tmem_ld_x32(taddr + uint32_t(c * 32), p);
+          tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
           store_col<32>(C, ldc, M, m0 + c * 32, n, v);
+        }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dempty[0]);
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue
@@ -620,7 +639,7 @@ __global__ void __launch_bounds__(Cfg<TM>::kThreads, Cfg<TM>::kMinBlocks)
 
 template <int TM, class OutT>
 cudaError_t launch_tm(const GemmW8A16Args& p, const DeviceInfo& dev, cudaStream_t stream) {
-  using Q = Cfg<TM>;
+  using Q = Cfg<TM, sizeof(OutT) == 4>;
   static bool attr_done[64] = {};
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
