@@ -443,6 +443,10 @@ __global__ void __launch_bounds__(Cfg<TM, sizeof(OutT) == 4>::kThreads, Cfg<TM, 
 #pragma unroll
         for (int c = 0; c < Q::kDecChunks; ++c)
           raw[c] = *reinterpret_cast<const uint4*>(wrow + (((c + c_first) ^ (row & 7)) << 4));
+        // The codes were read through the generic proxy and the stage is
+        // refilled by TMA (async proxy): without this fence the refill can
+        // overtake the reads (seen as wrong weight rows in whole tiles).
+        fence_async_shared();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         const bool got_a = __all_sync(0xffffffffu, mbar_wait(&aempty[a], aph ^ 1u, abort_flag));
@@ -478,13 +482,11 @@ __global__ void __launch_bounds__(Cfg<TM, sizeof(OutT) == 4>::kThreads, Cfg<TM, 
     // ------------------------------------------------------------ epilogue, UE8M0
     // The whole K range is in the one accumulator, and the tensor pipe waits
     // while it drains.  With bf16 output this warp reads all of its 64 token
-    // columns at once, stores them through its transpose buffer (a 2-byte
-    // store per thread and token took most of the time) and then releases the
-    // buffer.  (Releasing it between the reads and the stores, so that the
-    // next tile's MMAs overlap the stores, measured up to 8 % faster but gave
-    // wrong tiles in the last rounds of some runs on one GPU, a race whose
-    // cause is not found.)  Float output (64 more registers would spill) is
-    // read and stored 32 columns at a time.
+    // columns at once, releases the buffer, so that the next tile's MMAs
+    // overlap the stores, and then stores them through its transpose buffer
+    // (a 2-byte store per thread and token took most of the time).  Float
+    // output (64 more registers would spill) is read and stored 32 columns at
+    // a time and released after the stores.
     griddep_wait();   // the output may still be read or written by the previous kernel
     __nv_bfloat16* tr = reinterpret_cast<__nv_bfloat16*>(smem + Q::kRingBytes) +
                         (warp - kCtlWarps - Q::kDecWarps) * (32 * 32);
@@ -507,6 +509,9 @@ __global__ void __launch_bounds__(Cfg<TM, sizeof(OutT) == 4>::kThreads, Cfg<TM, 
         tmem_ld_x32(taddr, p);
         tmem_ld_x32(taddr + 32u, p + 32);
         tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[0]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float v[32];
@@ -526,10 +531,10 @@ __global__ void __launch_bounds__(Cfg<TM, sizeof(OutT) == 4>::kThreads, Cfg<TM, 
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(p[j]);
           store_col<32>(C, ldc, M, m0 + c * 32, n, v);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[0]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&dempty[0]);
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue

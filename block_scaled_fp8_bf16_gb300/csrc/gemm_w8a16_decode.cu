@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
       uint4 raw[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(wrow + ((c ^ (row & 7)) << 4));
+      fence_async_shared();   // generic-proxy reads of the stage come before its TMA (async-proxy) refill
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty[s]);   // the codes are in registers: the stage can refill
       s += kIssuers;

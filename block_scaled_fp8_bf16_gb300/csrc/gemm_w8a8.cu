@@ -408,6 +408,7 @@ __global__ void __launch_bounds__(W8A8Cfg<FUSED>::kThreads, 1)
           break;
         }
         const float sa = as_stage[s * BM + row_in_tile];
+        fence_async_shared();   // generic-proxy read of the stage before its TMA (async-proxy) refill
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         // The decision must be warp-uniform: tcgen05.ld below is .sync.aligned.

@@ -491,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float sa = as_stage[(j * kAsGroup + kr % kAsGroup) * TM + row];
         if (kr % kAsGroup == kAsGroup - 1 || kr == nkb - 1) {
+          fence_async_shared();   // generic-proxy reads of the scale stage before its TMA (async-proxy) refill
           __syncwarp();
           if (lane == 0) mbar_arrive(&as_empty[j]);
           ++gi;

@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm) quant_act_kernel(const
       uint4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(src + j * 64);
+      fence_async_shared();   // generic-proxy reads of the stage before its TMA (async-proxy) refill
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);   // the rows are in registers: the stage can refill
       float f[32];
