@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(Cfg<TM, sizeof(OutT) == 4>::kThreads, Cfg<TM, 
   // first token column of this epilogue warp (warps sharing a lane quarter split the columns)
   const int col0 = TM == 256 ? (warp >= kCtlWarps + Q::kDecWarps ? ((warp - kCtlWarps - Q::kDecWarps) >> 2) * EC : 0)
                              : (warp >= kCtlWarps + Q::kDecWarps + 4 ? EC : 0);
-  int last_nt = 0, last_mt = 0;
+  int last_nt = 0, last_mt = 0;   // the epilogue's last tile (one per cluster when K is split)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -605,14 +605,23 @@ __global__ void __launch_bounds__(Cfg<TM, sizeof(OutT) == 4>::kThreads, Cfg<TM, 
       for (int j = 0; j < EC; ++j) red[(col0 + j) * BN + row] = acc[j];
     }
     cluster_sync();
-    if (epi && !*abort_flag) {
-      const int et = (warp - kCtlWarps - Q::kDecWarps) * 32 + lane;   // 0 .. 32 * kEpiWarps - 1
-      constexpr int kTStep = 32 * Q::kEpiWarps / BN;          // token rows handled per pass
-      static_assert(32 * Q::kEpiWarps % BN == 0, "whole token rows per pass");
+    // With bf16 output the sum is shared by the whole CTA (the largest
+    // multiple of BN threads): the decode and control warps are idle by now,
+    // and with the epilogue warps alone it took 6-15 % longer on split
+    // shapes.  Float output keeps it on the epilogue warps (with all threads
+    // taking part, that instantiation no longer fits in its registers).
+    constexpr bool kAll = sizeof(OutT) == 2;
+    constexpr int kRedThreads = kAll ? (Q::kThreads / BN) * BN : 32 * Q::kEpiWarps;
+    static_assert(kRedThreads % BN == 0, "whole token rows per pass");
+    constexpr int kTStep = kRedThreads / BN;          // token rows handled per pass
+    const int et = kAll ? int(threadIdx.x) : (warp - kCtlWarps - Q::kDecWarps) * 32 + lane;
+    if ((kAll ? et < kRedThreads : epi) && !*abort_flag) {
       const int r_row = et % BN;
       const int t_end = (TM * (rank + 1)) / split;
-      const int m0 = last_mt * TM;
-      const int n0 = last_nt * BN;
+      int rnt = last_nt, rmt = last_mt;
+      if constexpr (kAll) tile_coords(cluster_id, n_tiles, m_tiles, rnt, rmt);   // one tile per cluster
+      const int m0 = rmt * TM;
+      const int n0 = rnt * BN;
       uint32_t base[kMaxSplitK];
 #pragma unroll
       for (int r = 0; r < kMaxSplitK; ++r)
