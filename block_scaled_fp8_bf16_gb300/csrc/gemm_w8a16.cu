@@ -126,7 +126,6 @@ __device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, 
   atomicCAS(err, 0, kDevErrW8A16 | site);
 }
 
-__device__ __forceinline__ __nv_bfloat16 to_out(float v, __nv_bfloat16*) { return __float2bfloat16_rn(v); }
 __device__ __forceinline__ float to_out(float v, float*) { return v; }
 
 template <int COLS, class OutT>
@@ -605,23 +604,58 @@ __global__ void __launch_bounds__(Cfg<TM, sizeof(OutT) == 4>::kThreads, Cfg<TM, 
       for (int j = 0; j < EC; ++j) red[(col0 + j) * BN + row] = acc[j];
     }
     cluster_sync();
-    // With bf16 output the sum is shared by the whole CTA (the largest
-    // multiple of BN threads): the decode and control warps are idle by now,
-    // and with the epilogue warps alone it took 6-15 % longer on split
-    // shapes.  Float output keeps it on the epilogue warps (with all threads
-    // taking part, that instantiation no longer fits in its registers).
+    // With bf16 output every thread of the CTA takes part (the decode and
+    // control warps are idle by now; with the epilogue warps alone the sum
+    // took 6-15 % longer on split shapes), each item being four weight rows
+    // of one token: 16-byte remote loads, 8-byte stores.  Float output keeps
+    // it on the epilogue warps, one value per thread (with all threads taking
+    // part, that instantiation no longer fits in its registers).
     constexpr bool kAll = sizeof(OutT) == 2;
-    constexpr int kRedThreads = kAll ? (Q::kThreads / BN) * BN : 32 * Q::kEpiWarps;
-    static_assert(kRedThreads % BN == 0, "whole token rows per pass");
-    constexpr int kTStep = kRedThreads / BN;          // token rows handled per pass
-    const int et = kAll ? int(threadIdx.x) : (warp - kCtlWarps - Q::kDecWarps) * 32 + lane;
-    if ((kAll ? et < kRedThreads : epi) && !*abort_flag) {
+    if constexpr (kAll) {
+      if (!*abort_flag) {
+        const int et = int(threadIdx.x);
+        int rnt, rmt;
+        tile_coords(cluster_id, n_tiles, m_tiles, rnt, rmt);   // one tile per cluster when K is split
+        const int m0 = rmt * TM;
+        const int n0 = rnt * BN;
+        const int t_begin = (TM * rank) / split;
+        const int items = ((TM * (rank + 1)) / split - t_begin) * (BN / 4);
+        const uint32_t red_addr = smem_u32(red);
+        for (int idx = et; idx < items; idx += Q::kThreads) {
+          const int t = t_begin + idx / (BN / 4);
+          const int r4 = 4 * (idx % (BN / 4));
+          if (m0 + t >= M) break;   // idx grows with t
+          const uint32_t off = red_addr + uint32_t(t * BN + r4) * 4u;
+          float4 v[kMaxSplitK];
+#pragma unroll
+          for (int r = 0; r < kMaxSplitK; ++r)
+            if (r < split) v[r] = ld_shared_cluster_f4(map_shared_rank(off, uint32_t(r)));
+          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int r = 0; r < kMaxSplitK; ++r) {
+            if (r < split) {   // rank order
+              sum.x += v[r].x;
+              sum.y += v[r].y;
+              sum.z += v[r].z;
+              sum.w += v[r].w;
+            }
+          }
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(sum.x, sum.y);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(sum.z, sum.w);
+          uint2 packed;
+          packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+          packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(C + size_t(m0 + t) * ldc + n0 + r4) = packed;
+        }
+      }
+    } else if (epi && !*abort_flag) {
+      const int et = (warp - kCtlWarps - Q::kDecWarps) * 32 + lane;   // 0 .. 32 * kEpiWarps - 1
+      constexpr int kTStep = 32 * Q::kEpiWarps / BN;          // token rows handled per pass
+      static_assert(32 * Q::kEpiWarps % BN == 0, "whole token rows per pass");
       const int r_row = et % BN;
       const int t_end = (TM * (rank + 1)) / split;
-      int rnt = last_nt, rmt = last_mt;
-      if constexpr (kAll) tile_coords(cluster_id, n_tiles, m_tiles, rnt, rmt);   // one tile per cluster
-      const int m0 = rmt * TM;
-      const int n0 = rnt * BN;
+      const int m0 = last_mt * TM;
+      const int n0 = last_nt * BN;
       uint32_t base[kMaxSplitK];
 #pragma unroll
       for (int r = 0; r < kMaxSplitK; ++r)
