@@ -122,6 +122,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 __device__ __forceinline__ __nv_bfloat16 to_out(float v, __nv_bfloat16*) { return __float2bfloat16_rn(v); }
 __device__ __forceinline__ float to_out(float v, float*) { return v; }
 
+// Four consecutive outputs of one row (the address is 8-byte aligned for bf16, 16-byte for float).
+__device__ __forceinline__ void store4(__nv_bfloat16* dst, const float4& v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 packed;
+  packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+  packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dst) = packed;
+}
+__device__ __forceinline__ void store4(float* dst, const float4& v) { *reinterpret_cast<float4*>(dst) = v; }
+
 // OutT: __nv_bfloat16 (rounded to nearest even) or float (the accumulator as is).
 template <int TM, class OutT>
 __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
@@ -401,20 +412,30 @@ __global__ void __launch_bounds__(DecCfg<TM>::kThreads, 1)
         raise_error(err, abort_flag, kSiteReduceFull);
         return false;
       }
+      // Items of four consecutive weight rows of one token: 16-byte remote
+      // loads and one 8-byte (bf16) or 16-byte (float) store each.
       const int rows = BN / split;
-      const int rl = et % rows;
-      const int n_out = (cluster_id + q * num_clusters) * BN + rank * rows + rl;
-      for (int m = et / rows; m < M; m += split) {
-        const uint32_t local = smem_u32(rb + m * BN + rank * rows + rl);
-        float v[kMaxSplitK];
+      const int quads = rows / 4;
+      const int n_base = (cluster_id + q * num_clusters) * BN + rank * rows;
+      for (int idx = et; idx < M * quads; idx += 32 * kEpiWarps) {
+        const int m = idx / quads;
+        const int r4 = 4 * (idx % quads);
+        const uint32_t local = smem_u32(rb + m * BN + rank * rows + r4);
+        float4 v[kMaxSplitK];
 #pragma unroll
         for (int r = 0; r < kMaxSplitK; ++r)
-          if (r < split) v[r] = ld_dsmem_f32(map_shared_rank(local, uint32_t(r)));
-        float sum = 0.f;
+          if (r < split) v[r] = ld_shared_cluster_f4(map_shared_rank(local, uint32_t(r)));
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int r = 0; r < kMaxSplitK; ++r)
-          if (r < split) sum += v[r];
-        C[size_t(m) * ldc + n_out] = to_out(sum, C);
+        for (int r = 0; r < kMaxSplitK; ++r) {
+          if (r < split) {   // rank order
+            sum.x += v[r].x;
+            sum.y += v[r].y;
+            sum.z += v[r].z;
+            sum.w += v[r].w;
+          }
+        }
+        store4(C + size_t(m) * ldc + n_base + r4, sum);
       }
       __syncwarp();
       if (lane == 0) {
