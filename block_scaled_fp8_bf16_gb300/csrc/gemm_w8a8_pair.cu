@@ -128,22 +128,33 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
 // halves the length of that round; when all tiles fit on half of the pairs
 // (the launch then gives two pairs per tile), every tile runs as two halves.
 // Items [0, full_items) are whole tiles; item full_items + 2u + h is half h
-// of tile full_items + u.  half = -1 marks a whole tile.
+// of tile full_items + u.  half = -1 marks a whole tile.  Grouped problems
+// add, from item pass1 on, a second pass over every tile (whole), for the
+// group of its second 128-row half when that differs from the first's; the
+// first passes are scheduled like a dense problem (halves in a last round
+// that would fill at most half of the pairs).
 struct Items {
-  int full_items, num_items;
+  int full_items, num_items, pass1;
 };
 __device__ __forceinline__ Items make_items(int num_tiles, int num_pairs, bool grouped) {
-  if (grouped) return Items{2 * num_tiles, 2 * num_tiles};   // two passes per tile, no half tiles
-  if (2 * num_tiles <= num_pairs) return Items{0, 2 * num_tiles};
-  const int rem = num_tiles % num_pairs;
-  const int split = (num_tiles > num_pairs && rem > 0 && 2 * rem <= num_pairs) ? rem : 0;
-  return Items{num_tiles - split, num_tiles + split};
+  Items it;
+  if (2 * num_tiles <= num_pairs) {
+    it.full_items = 0;
+    it.num_items = 2 * num_tiles;
+  } else {
+    const int rem = num_tiles % num_pairs;
+    const int split = (num_tiles > num_pairs && rem > 0 && 2 * rem <= num_pairs) ? rem : 0;
+    it.full_items = num_tiles - split;
+    it.num_items = num_tiles + split;
+  }
+  it.pass1 = it.num_items;
+  if (grouped) it.num_items += num_tiles;
+  return it;
 }
-__device__ __forceinline__ void item_coords(int t, const Items& items, int m_tiles, int n_tiles, bool grouped,
-                                            int& mt, int& nt, int& half) {
-  if (grouped) {
-    // item t is pass t / num_tiles of tile t % num_tiles
-    tile_coords(t % (m_tiles * n_tiles), m_tiles, n_tiles, mt, nt);
+__device__ __forceinline__ void item_coords(int t, const Items& items, int m_tiles, int n_tiles, int& mt, int& nt,
+                                            int& half) {
+  if (t >= items.pass1) {
+    tile_coords(t - items.pass1, m_tiles, n_tiles, mt, nt);   // grouped second pass, whole tile
     half = -1;
   } else if (t < items.full_items) {
     tile_coords(t, m_tiles, n_tiles, mt, nt);
@@ -165,15 +176,16 @@ __device__ __forceinline__ int half_group(const int* row_group, int r, int M) {
   return r < M ? __ldg(row_group + r) : -1;
 }
 
-// Grouped: the group that item t's pass multiplies with (pass t / num_tiles
-// of pair tile row mt), or -1 when the pass has no rows to compute (padding,
-// a second half of the same group, or a group past the weights).  Dense
-// problems: 0.
-__device__ __forceinline__ int item_group(const int* row_group, int G, int M, int t, int num_tiles, int mt) {
+// Grouped: the group that item t's pass multiplies with (the first pass,
+// items before pass1, takes the group of the pair tile row's first half, the
+// second pass that of its second half), or -1 when the pass has no rows to
+// compute (padding, a second half of the same group, or a group past the
+// weights).  Dense problems: 0.
+__device__ __forceinline__ int item_group(const int* row_group, int G, int M, int t, int pass1, int mt) {
   if (row_group == nullptr) return 0;
   const int g0 = half_group(row_group, mt * 2 * TM, M);
   const int g1 = half_group(row_group, mt * 2 * TM + TM, M);
-  const int g = t < num_tiles ? g0 : (g1 != g0 ? g1 : -1);
+  const int g = t < pass1 ? g0 : (g1 != g0 ? g1 : -1);
   return g < G ? g : -1;
 }
 
@@ -243,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   // The epilogue re-reads the item counts from here at each tile instead of
   // keeping them in registers across its K loop.
-  volatile int* items_sh = abort_flag + 1;   // full_items, num_items
+  volatile int* items_sh = abort_flag + 1;   // full_items, num_items, pass1
 
   griddep_launch_dependents();   // the next kernel may start its prologue; it gets an SM when this CTA leaves
 
@@ -283,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     items_sh[0] = items.full_items;
     items_sh[1] = items.num_items;
+    items_sh[2] = items.pass1;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -316,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = pair; t < items.num_items && ok; t += num_pairs) {
         int mt, nt, half;
-        item_coords(t, items, m_tiles, n_tiles, row_group != nullptr, mt, nt, half);
-        const int g = item_group(row_group, G, M, t, num_tiles, mt);
+        item_coords(t, items, m_tiles, n_tiles, mt, nt, half);
+        const int g = item_group(row_group, G, M, t, items.pass1, mt);
         if (g < 0) continue;
         const int m0 = mt * 2 * TM + rank * TM;
         // A half tile's MMA reads the first 64 of this CTA's B rows: rows
@@ -383,10 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = pair; t < items.num_items && ok; t += num_pairs) {
         if (row_group != nullptr) {
           int mt, nt, half;
-          item_coords(t, items, m_tiles, n_tiles, true, mt, nt, half);
-          if (item_group(row_group, G, M, t, num_tiles, mt) < 0) continue;
+          item_coords(t, items, m_tiles, n_tiles, mt, nt, half);
+          if (item_group(row_group, G, M, t, items.pass1, mt) < 0) continue;
         }
-        const uint32_t idesc = t < items.full_items ? kIdesc : kIdescHalf;
+        const uint32_t idesc = (t < items.full_items || t >= items.pass1) ? kIdesc : kIdescHalf;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           if ((it & 1u) != w) continue;
           const int s = it % kStages;
@@ -528,11 +541,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (y < M && col_ok && store) store_block(nc_tag, y, n);
     };
     for (int t = pair; ok; t += num_pairs) {
-      const Items it_sh{items_sh[0], items_sh[1]};
+      const Items it_sh{items_sh[0], items_sh[1], items_sh[2]};
       if (t >= it_sh.num_items) break;
       int mt, nt, half;
-      item_coords(t, it_sh, m_tiles, n_tiles, row_group != nullptr, mt, nt, half);
-      const int g = item_group(row_group, G, M, t, num_tiles, mt);
+      item_coords(t, it_sh, m_tiles, n_tiles, mt, nt, half);
+      const int g = item_group(row_group, G, M, t, it_sh.pass1, mt);
       if (g < 0) {
         // A group index past the weights in this CTA's rows: skipped and
         // reported (by one thread).

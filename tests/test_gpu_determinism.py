@@ -44,6 +44,7 @@ def test_w8a8_deterministic(lib, M, N, K):
 @pytest.mark.parametrize("groups,rows,N,K", [
     (4, 512, 2048, 1024),  # CTA pairs (groups of at least 256 rows)
     (8, 128, 1024, 1024),  # single CTA (128-row groups)
+    (4, 384, 4096, 512),   # CTA pairs: halves in the last round, second passes for tiles holding two groups
 ])
 def test_w8a8_grouped_deterministic(lib, groups, rows, N, K):
     M = groups * rows

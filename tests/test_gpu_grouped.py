@@ -56,6 +56,9 @@ def run_grouped(lib, a, As, b, Bs, row_group, dtype=torch.bfloat16):
     ((3, 4, 1, 6, 2), 2048, 512, (0, 7), torch.float32),
     ((4, 2, 6), 4096, 384, (), torch.bfloat16),
     ((1, 3, 2, 5, 1, 4), 2048, 1024, (1, 12), torch.bfloat16),
+    # 96 pair tiles on 76 pairs: the first passes' last round runs as 256 x 128
+    # halves, and groups of 384 and 640 rows give pair tiles a second pass
+    ((3, 4, 5), 4096, 256, (), torch.bfloat16),
 ])
 def test_grouped_matches_oracle(lib, tiles, N, K, pads, dtype):
     a, As, b, Bs, g = grouped_inputs(sum(tiles) + N + K, tiles, N, K, pads)
